@@ -1,0 +1,237 @@
+"""ctypes binding of libmoe.so: the same calls as include/moe.h, on torch tensors.
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  PyTorch provides device memory and the current stream.  If
+libmoe.so is missing or cannot be loaded, importing this module raises; there
+is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+P = ctypes.c_void_p
+I = ctypes.c_int
+I64 = ctypes.c_int64
+SZ = ctypes.c_size_t
+
+MOE_DTYPE_BF16 = 0
+MOE_DTYPE_F32 = 1
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
+          6: "MOE_ERR_DEVICE_CHECK", 7: "MOE_ERR_TIMEOUT"}
+
+_SIGS = {
+    "moe_status_string": ([I], ctypes.c_char_p),
+    "moe_version": ([], I),
+    "moe_router_logits": ([P, P, P, I, I, I, P, P], I),
+    "moe_route": ([P, I, I, I, I, P, P, P, P], I),
+    "moe_permute_workspace_size": ([I, I, I, I], SZ),
+    "moe_permute": ([P, I, I, I, I, P, I, I, P, P, P, P, P, SZ, P, P], I),
+    "moe_ffn_workspace_size": ([I, I], SZ),
+    "moe_grouped_gemm_swiglu": ([P, P, I, I, I, I, P, P, P, P, SZ, P, P], I),
+    "moe_grouped_gemv": ([P, P, I, I, I, I, P, P, P, P, SZ, P, P], I),
+    "moe_grouped_gemm_swiglu_w8": ([P, P, I, I, I, I, P, P, P, P, P, P, SZ, P, P], I),
+    "moe_grouped_gemv_w8": ([P, P, I, I, I, I, P, P, P, P, P, P, SZ, P, P], I),
+    "moe_combine": ([P, P, P, I, I, I, I, P, P, P, P], I),
+    "moe_quantize_w8": ([P, I64, I64, P, P], I),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.moe_status_string(status).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def _ok(status: int, where: str) -> None:
+    if status != 0:
+        raise MoEError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def version() -> int:
+    return int(_lib.moe_version())
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_status_string(status).decode()
+
+
+def new_error_word(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_device_error(err: torch.Tensor, where: str = "device check") -> None:
+    """Synchronise on the word's device and raise if a kernel stored an error."""
+    v = int(err.item())
+    if v != 0:
+        raise MoEError(v, where)
+
+
+# --------------------------------------------------------------------- calls
+
+def moe_router_logits(x, w_r, bias, logits, stream=None):
+    T, H = x.shape
+    E = w_r.shape[0]
+    _dev(x, "x", torch.bfloat16); _dev(w_r, "w_r", torch.bfloat16)
+    _dev(logits, "logits", torch.float32)
+    if bias is not None:
+        _dev(bias, "bias", torch.float32)
+    _ok(_lib.moe_router_logits(_ptr(x), _ptr(w_r), _ptr(bias), T, H, E, _ptr(logits),
+                               _stream(stream)), "moe_router_logits")
+
+
+def moe_route(logits, k, renormalize, topk_ids, topk_w, dev_error=None, stream=None):
+    _dev(logits, "logits", torch.float32)
+    T, E = logits.shape
+    _dev(topk_ids, "topk_ids", torch.int32); _dev(topk_w, "topk_w", torch.float32)
+    _ok(_lib.moe_route(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(topk_ids),
+                       _ptr(topk_w), _ptr(dev_error), _stream(stream)), "moe_route")
+
+
+def moe_permute_workspace_size(T, E, S, k) -> int:
+    return int(_lib.moe_permute_workspace_size(T, E, S, k))
+
+
+def moe_permute(topk_ids, E, S, x, offsets, sorted_slot, row_of_slot, x_perm, workspace=None,
+                dev_error=None, stream=None):
+    _dev(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    _dev(x, "x")
+    if x.dtype == torch.bfloat16:
+        xd = MOE_DTYPE_BF16
+    elif x.dtype == torch.float32:
+        xd = MOE_DTYPE_F32
+    else:
+        raise ValueError("x must be bf16 or fp32")
+    H = x.shape[1]
+    for n, t in (("offsets", offsets), ("sorted_slot", sorted_slot),
+                 ("row_of_slot", row_of_slot)):
+        _dev(t, n, torch.int32)
+    _dev(x_perm, "x_perm", torch.bfloat16)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(_lib.moe_permute(_ptr(topk_ids), T, E, S, k, _ptr(x), xd, H, _ptr(offsets),
+                         _ptr(sorted_slot), _ptr(row_of_slot), _ptr(x_perm), _ptr(workspace),
+                         wsb, _ptr(dev_error), _stream(stream)), "moe_permute")
+
+
+def moe_ffn_workspace_size(M, I) -> int:
+    return int(_lib.moe_ffn_workspace_size(M, I))
+
+
+def _ffn_common(x_perm, offsets, y_perm, workspace):
+    _dev(x_perm, "x_perm", torch.bfloat16); _dev(offsets, "offsets", torch.int32)
+    _dev(y_perm, "y_perm", torch.bfloat16); _dev(workspace, "workspace")
+    M, H = x_perm.shape
+    G = offsets.numel() - 1
+    return M, H, G, workspace.numel() * workspace.element_size()
+
+
+def moe_grouped_gemm_swiglu(x_perm, offsets, w_gu, w_down, y_perm, workspace, dev_error=None,
+                            stream=None):
+    M, H, G, wsb = _ffn_common(x_perm, offsets, y_perm, workspace)
+    _dev(w_gu, "w_gu", torch.bfloat16); _dev(w_down, "w_down", torch.bfloat16)
+    I_ = w_down.shape[2]
+    _ok(_lib.moe_grouped_gemm_swiglu(_ptr(x_perm), _ptr(offsets), G, M, H, I_, _ptr(w_gu),
+                                     _ptr(w_down), _ptr(y_perm), _ptr(workspace), wsb,
+                                     _ptr(dev_error), _stream(stream)), "moe_grouped_gemm_swiglu")
+
+
+def moe_grouped_gemv(x_perm, offsets, w_gu, w_down, y_perm, workspace, dev_error=None,
+                     stream=None):
+    M, H, G, wsb = _ffn_common(x_perm, offsets, y_perm, workspace)
+    _dev(w_gu, "w_gu", torch.bfloat16); _dev(w_down, "w_down", torch.bfloat16)
+    I_ = w_down.shape[2]
+    _ok(_lib.moe_grouped_gemv(_ptr(x_perm), _ptr(offsets), G, M, H, I_, _ptr(w_gu),
+                              _ptr(w_down), _ptr(y_perm), _ptr(workspace), wsb, _ptr(dev_error),
+                              _stream(stream)), "moe_grouped_gemv")
+
+
+def moe_grouped_gemm_swiglu_w8(x_perm, offsets, q_gu, s_gu, q_down, s_down, y_perm, workspace,
+                               dev_error=None, stream=None):
+    M, H, G, wsb = _ffn_common(x_perm, offsets, y_perm, workspace)
+    for n, t, d in (("q_gu", q_gu, torch.int8), ("s_gu", s_gu, torch.float32),
+                    ("q_down", q_down, torch.int8), ("s_down", s_down, torch.float32)):
+        _dev(t, n, d)
+    I_ = q_down.shape[2]
+    _ok(_lib.moe_grouped_gemm_swiglu_w8(_ptr(x_perm), _ptr(offsets), G, M, H, I_, _ptr(q_gu),
+                                        _ptr(s_gu), _ptr(q_down), _ptr(s_down), _ptr(y_perm),
+                                        _ptr(workspace), wsb, _ptr(dev_error), _stream(stream)),
+        "moe_grouped_gemm_swiglu_w8")
+
+
+def moe_grouped_gemv_w8(x_perm, offsets, q_gu, s_gu, q_down, s_down, y_perm, workspace,
+                        dev_error=None, stream=None):
+    M, H, G, wsb = _ffn_common(x_perm, offsets, y_perm, workspace)
+    for n, t, d in (("q_gu", q_gu, torch.int8), ("s_gu", s_gu, torch.float32),
+                    ("q_down", q_down, torch.int8), ("s_down", s_down, torch.float32)):
+        _dev(t, n, d)
+    I_ = q_down.shape[2]
+    _ok(_lib.moe_grouped_gemv_w8(_ptr(x_perm), _ptr(offsets), G, M, H, I_, _ptr(q_gu),
+                                 _ptr(s_gu), _ptr(q_down), _ptr(s_down), _ptr(y_perm),
+                                 _ptr(workspace), wsb, _ptr(dev_error), _stream(stream)),
+        "moe_grouped_gemv_w8")
+
+
+def moe_combine(y_perm, row_of_slot, topk_w, S, out, residual=None, dev_error=None,
+                stream=None):
+    _dev(y_perm, "y_perm", torch.bfloat16); _dev(row_of_slot, "row_of_slot", torch.int32)
+    _dev(topk_w, "topk_w", torch.float32); _dev(out, "out", torch.bfloat16)
+    if residual is not None:
+        _dev(residual, "residual", torch.bfloat16)
+    T, k = topk_w.shape
+    H = out.shape[1]
+    _ok(_lib.moe_combine(_ptr(y_perm), _ptr(row_of_slot), _ptr(topk_w), T, k, S, H,
+                         _ptr(residual), _ptr(out), _ptr(dev_error), _stream(stream)),
+        "moe_combine")
+
+
+def moe_quantize_w8(w: torch.Tensor):
+    """Host-side int8 quantisation of a bf16 tensor [..., K] (any device;
+    the work runs on host copies).  Returns (q int8, scale fp32) on the CPU."""
+    wc = w.detach().to("cpu").contiguous()
+    if wc.dtype != torch.bfloat16:
+        raise ValueError("w must be bf16")
+    K = wc.shape[-1]
+    rows = wc.numel() // K
+    q = torch.empty(wc.shape, dtype=torch.int8)
+    s = torch.empty(wc.shape[:-1], dtype=torch.float32)
+    _ok(_lib.moe_quantize_w8(_ptr(wc), rows, K, _ptr(q), _ptr(s)), "moe_quantize_w8")
+    return q, s

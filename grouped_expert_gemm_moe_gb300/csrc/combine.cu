@@ -1,0 +1,82 @@
+// combine.cu -- gather-based weighted combine back to token order.
+//
+// Each output chunk of 8 hidden elements gathers its token's k routed rows
+// (and S shared rows) from y_perm and sums them in fp32 in a fixed order,
+// so the result is the same bytes on every run.  The "dispatch" project's
+// Phase 6 pull request (Summary) had to widen a repeatability check because
+// its index_add_ (atomicAdd) combine is not bitwise deterministic; a gather
+// has no such race.
+#include "common.cuh"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256) combine_kernel(
+    const uint16_t *__restrict__ y_perm, const int32_t *__restrict__ row_of_slot,
+    const float *__restrict__ topk_w, int T, int k, int S, int H,
+    const uint16_t *residual, uint16_t *out, int32_t *dev_error) {
+    const int t = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;     // 8-element chunk
+    if (c * 8 >= H) return;
+    const int64_t n = static_cast<int64_t>(T) * k;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+
+    auto add_row = [&](int64_t r, float w) {
+        const uint4 v = ld_nc(y_perm + r * H + c * 8);
+        const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(w, bf_lo(p[i]), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(w, bf_hi(p[i]), acc[2 * i + 1]);
+        }
+    };
+    for (int j = 0; j < k; ++j) {
+        const int64_t slot = static_cast<int64_t>(t) * k + j;
+        const int64_t r = row_of_slot[slot];
+        if (r < 0 || r >= n) {
+            report(dev_error, MOE_ERR_DEVICE_CHECK);
+            continue;
+        }
+        add_row(r, topk_w[slot]);
+    }
+    for (int s = 0; s < S; ++s) add_row(n + static_cast<int64_t>(s) * T + t, 1.0f);
+    if (residual) {
+        const uint4 v = ld_nc(residual + static_cast<int64_t>(t) * H + c * 8);
+        const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += bf_lo(p[i]);
+            acc[2 * i + 1] += bf_hi(p[i]);
+        }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(t) * H + c * 8) = o;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_slot,
+                                  const float *topk_w, int T, int k, int S, int H,
+                                  const uint16_t *residual, uint16_t *out, int32_t *dev_error,
+                                  cudaStream_t stream) {
+    if (!y_perm || !row_of_slot || !topk_w || !out || T < 1 || k < 1 || k > 32 || S < 0 || H < 1)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t M = static_cast<int64_t>(T) * k + static_cast<int64_t>(S) * T;
+    if (M * H >= (1ll << 31) || T > 65535 * 64) return MOE_ERR_UNSUPPORTED;
+    if (H % 8 != 0 || !aligned16(y_perm) || !aligned16(out) || (residual && !aligned16(residual)))
+        return MOE_ERR_ALIGNMENT;
+    if (T > 65535) return MOE_ERR_UNSUPPORTED;   // grid.y limit
+    const int chunks = H / 8;
+    const int threads = chunks >= 256 ? 256 : ((chunks + 31) / 32) * 32;
+    dim3 grid((chunks + threads - 1) / threads, T);
+    combine_kernel<<<grid, threads, 0, stream>>>(y_perm, row_of_slot, topk_w, T, k, S, H, residual,
+                                                 out, dev_error);
+    return launch_status();
+}

@@ -1,0 +1,395 @@
+// gemm_tc.cu -- all-experts grouped GEMM on the 5th-generation tensor cores.
+//
+// "A tensor-core grouped GEMM with SwiGLU fused into its epilogue", all
+// experts in one launch ("switchyard" page, 02 Kernels and dispatch, "One
+// launch for all experts").  Written for sm_103a:
+//
+//  * persistent grid, one CTA per SM; a per-expert tile scheduler walks the
+//    linear tile index over (group g, n-tile, m-tile) with the m-tile
+//    fastest, so CTAs that run at the same time read the same weight tile
+//    (one HBM read, the rest L2 hits).  The tile table is built on the
+//    device from the offsets table: the host never learns the group sizes;
+//  * warp 0: TMA producer (one thread) filling a ring of STAGES shared
+//    memory stages: the activation tile (token rows, K-major, 128-byte
+//    swizzle, fetched as 16-row boxes so a small group only pulls the rows
+//    it has) and the weight tile;
+//  * warp 1: TMEM allocator and MMA issuer (one thread): tcgen05.mma
+//    kind::f16, M = 128 token rows, N = BN weight rows, K = 16 per
+//    instruction, fp32 accumulators in TMEM, double-buffered (2 x BN
+//    columns) so the epilogue of one tile overlaps the main loop of the next;
+//  * warps 2-5: epilogue.  tcgen05.ld moves a thread's accumulator row into
+//    registers; SWIGLU mode holds gate rows n0..n0+BN/2-1 in accumulator
+//    columns [0, BN/2) and the matching up rows in [BN/2, BN), so
+//    h = silu(gate) * up is formed in registers and stored as bf16; PLAIN
+//    mode stores the accumulator as bf16.
+// Every mbarrier wait is bounded (1 s); on running out the kernel records
+// MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <algorithm>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int TC_BM = 128;        // token rows per tile (MMA M)
+constexpr int TC_BK = 64;         // K per stage: one 128-byte swizzle row of bf16
+constexpr int TC_THREADS = 192;   // 6 warps
+constexpr int TC_ABOX = 16;       // rows per activation TMA box
+
+template <int BN>
+struct TcCfg {
+    static constexpr int A_BYTES = TC_BM * TC_BK * 2;
+    static constexpr int B_BYTES = BN * TC_BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static size_t smem_bytes(int G) {
+        return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES +
+               2 * static_cast<size_t>(G + 1) * sizeof(int);
+    }
+};
+
+struct TileInfo {
+    int g, nt, m0, nrows;
+};
+
+// s_tile[g] = first linear tile of group g (s_tile[G] = total).
+__device__ __forceinline__ TileInfo decode_tile(int t, const int *s_tile, const int *s_off, int G) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tile[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.g = lo;
+    const int u = t - s_tile[lo];
+    const int rows = s_off[lo + 1] - s_off[lo];
+    const int mt_count = (rows + TC_BM - 1) / TC_BM;
+    ti.nt = u / mt_count;
+    const int mt = u - ti.nt * mt_count;
+    ti.m0 = s_off[lo] + mt * TC_BM;
+    ti.nrows = min(TC_BM, rows - mt * TC_BM);
+    return ti;
+}
+
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// SWIGLU: out = h [M, NOUT=I], weights [G*2I, K=H], up rows at +UP_OFF = I.
+// PLAIN : out = y [M, NOUT=H], weights [G*H,  K=I].
+template <bool SWIGLU, int BN>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_w, const int32_t *__restrict__ offsets,
+                    int G, int M, int K, int R, int NOUT, int UP_OFF, uint16_t *__restrict__ out,
+                    int32_t *dev_error) {
+    using C = TcCfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * C::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *accf = empty + STAGES;
+    uint64_t *acce = accf + 2;
+    uint64_t *drain = acce + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    int *s_total = reinterpret_cast<int *>(tmem_slot + 1);
+    int *s_off = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(full) + C::BAR_BYTES);
+    int *s_tile = s_off + (G + 1);
+
+    const int warp = threadIdx.x >> 5, lane = lane_id();
+    const int n_per_tile = SWIGLU ? BN / 2 : BN;
+    const int n_tiles = (NOUT + n_per_tile - 1) / n_per_tile;
+    const int KB = (K + TC_BK - 1) / TC_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 128);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_w);
+    }
+    if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
+    if (warp == 2) {
+        // tile table: tiles of group g = n_tiles * ceil(rows_g / 128)
+        int carry = 0;
+        bool bad = false;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int tiles = 0;
+            if (g < G) {
+                const int o0 = offsets[g], o1 = offsets[g + 1];
+                if (o0 < 0 || o1 < o0 || o1 > M) bad = true;
+                else tiles = ((o1 - o0 + TC_BM - 1) / TC_BM) * n_tiles;
+                s_off[g] = o0;
+                if (g == G - 1) s_off[G] = o1;
+            }
+            const int inc = warp_inclusive_scan(tiles);
+            if (g < G) s_tile[g] = carry + inc - tiles;
+            carry += __shfl_sync(FULL, inc, 31);
+        }
+        bad = __any_sync(FULL, bad);
+        if (lane == 0) {
+            s_tile[G] = carry;
+            *s_total = bad ? 0 : carry;
+            if (bad) report(dev_error, MOE_ERR_DEVICE_CHECK);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = *s_total;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;     // per stage: ever filled / parity of last fill
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_tile, s_off, G);
+                const int nbox = (ti.nrows + TC_ABOX - 1) / TC_ABOX;
+                const uint32_t bytes = nbox * TC_ABOX * TC_BK * 2 + C::B_BYTES;
+                const int wrow = ti.g * R + ti.nt * n_per_tile;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, dev_error)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    uint8_t *a = sA + stage * C::A_BYTES;
+                    uint8_t *b = sB + stage * C::B_BYTES;
+                    const int kx = kb * TC_BK;
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_load_2d(a + bx * TC_ABOX * 128, &tm_act, &full[stage], kx,
+                                    ti.m0 + bx * TC_ABOX, pol_a);
+                    if (SWIGLU) {
+                        tma_load_2d(b, &tm_w, &full[stage], kx, wrow, pol_w);
+                        tma_load_2d(b + (BN / 2) * 128, &tm_w, &full[stage], kx, wrow + UP_OFF,
+                                    pol_w);
+                    } else {
+                        tma_load_2d(b, &tm_w, &full[stage], kx, wrow, pol_w);
+                    }
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // drain: every copy this thread issued has landed before exit
+            for (int s = 0; s < STAGES; ++s)
+                if ((filled >> s) & 1u) mbar_wait(&full[s], (fill_parity >> s) & 1u, dev_error);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (!mbar_wait(&acce[acc], acc_phase ^ 1u, dev_error)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, dev_error)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < TC_BK / 16; ++kk)
+                        tc_mma_bf16(d_tmem, sw128_kmajor_desc(a_addr + kk * 32),
+                                    sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&accf[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // drain: every MMA this thread issued has completed before exit
+            tc_commit(drain);
+            mbar_wait(drain, 0, dev_error);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int quarter = warp & 3;       // TMEM lanes this warp may access
+        const int row_in_tile = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const TileInfo ti = decode_tile(t, s_tile, s_off, G);
+            if (!mbar_wait(&accf[acc], acc_phase, dev_error)) break;
+            tc_fence_after();
+            const bool valid = row_in_tile < ti.nrows;
+            uint16_t *orow = out + static_cast<int64_t>(ti.m0 + row_in_tile) * NOUT;
+            const uint32_t tbase =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+            const int n0 = ti.nt * n_per_tile;
+            if (SWIGLU) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 16) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tbase + c, g);
+                    tmem_ld16(tbase + BN / 2 + c, u);
+                    tmem_ld_wait();
+                    if (valid && n0 + c < NOUT) {
+                        uint32_t p[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float h0 = silu_fast(__uint_as_float(g[2 * i])) *
+                                             __uint_as_float(u[2 * i]);
+                            const float h1 = silu_fast(__uint_as_float(g[2 * i + 1])) *
+                                             __uint_as_float(u[2 * i + 1]);
+                            p[i] = pack_bf16x2(h0, h1);
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c);
+                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                        if (n0 + c + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tbase + c, v);
+                    tmem_ld_wait();
+                    if (valid && n0 + c < NOUT) {
+                        uint32_t p[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            p[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
+                                               __uint_as_float(v[2 * i + 1]));
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c);
+                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                        if (n0 + c + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acce[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<C::TMEM_COLS>(tmem_base);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] row-major, box [box_outer, 64], 128-byte swizzle.
+static bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                           uint32_t box_outer) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(TC_BK), box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SWIGLU, int BN>
+static moe_status launch_tc(const void *act, const void *w, const int32_t *offsets, int G, int M,
+                            int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
+                            cudaStream_t stream) {
+    CUtensorMap tm_act, tm_w;
+    if (!encode_bf16_2d(&tm_act, act, K, M, TC_ABOX)) return MOE_ERR_CUDA;
+    if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, SWIGLU ? BN / 2 : BN))
+        return MOE_ERR_CUDA;
+    const size_t smem = TcCfg<BN>::smem_bytes(G);
+    if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(tc_grouped_gemm<SWIGLU, BN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    tc_grouped_gemm<SWIGLU, BN><<<sm_count(), TC_THREADS, smem, stream>>>(
+        tm_act, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
+    return launch_status();
+}
+
+moe_status check_ffn_args(const void *x_perm, const int32_t *offsets, int G, int M, int H, int I,
+                          const void *w_gu, const void *w_down, const void *y_perm,
+                          const void *workspace, size_t workspace_bytes, int k_align);
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_grouped_gemm_swiglu(const uint16_t *x_perm, const int32_t *offsets,
+                                              int G, int M, int H, int I, const uint16_t *w_gu,
+                                              const uint16_t *w_down, uint16_t *y_perm,
+                                              void *workspace, size_t workspace_bytes,
+                                              int32_t *dev_error, cudaStream_t stream) {
+    moe_status st = check_ffn_args(x_perm, offsets, G, M, H, I, w_gu, w_down, y_perm, workspace,
+                                   workspace_bytes, 8);
+    if (st != MOE_OK) return st;
+    uint16_t *h = static_cast<uint16_t *>(workspace);
+    st = launch_tc<true, 256>(x_perm, w_gu, offsets, G, M, H, 2 * I, I, I, h, dev_error, stream);
+    if (st != MOE_OK) return st;
+    return launch_tc<false, 256>(h, w_down, offsets, G, M, I, H, H, 0, y_perm, dev_error, stream);
+}
+
+extern "C" moe_status moe_grouped_gemm_swiglu_w8(const uint16_t *x_perm, const int32_t *offsets,
+                                                 int G, int M, int H, int I, const int8_t *q_gu,
+                                                 const float *s_gu, const int8_t *q_down,
+                                                 const float *s_down, uint16_t *y_perm,
+                                                 void *workspace, size_t workspace_bytes,
+                                                 int32_t *dev_error, cudaStream_t stream) {
+    (void)x_perm; (void)offsets; (void)G; (void)M; (void)H; (void)I; (void)q_gu; (void)s_gu;
+    (void)q_down; (void)s_down; (void)y_perm; (void)workspace; (void)workspace_bytes;
+    (void)dev_error; (void)stream;
+    return MOE_ERR_UNSUPPORTED;
+}

@@ -1,0 +1,154 @@
+"""One MoE layer (and a stack of them) on top of the C-ABI calls.
+
+``MoELayer.forward`` runs route -> permute -> grouped FFN -> combine on the
+current CUDA stream, with every buffer preallocated by PyTorch and reused
+across calls, so a forward pass allocates nothing and launches only this
+library's kernels.  The grouped FFN is the tcgen05 grouped GEMM, or the
+grouped GEMV when the batch has only a few rows per expert.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import binding as B
+
+# Mean permuted rows per expert group at or below which the grouped GEMV is
+# used instead of the tensor-core grouped GEMM.
+GEMV_MAX_ROWS_PER_GROUP = 2.0
+
+
+@dataclass
+class LayerBuffers:
+    T: int
+    topk_ids: torch.Tensor
+    topk_w: torch.Tensor
+    offsets: torch.Tensor
+    sorted_slot: torch.Tensor
+    row_of_slot: torch.Tensor
+    x_perm: torch.Tensor
+    y_perm: torch.Tensor
+    ffn_ws: torch.Tensor
+    out: torch.Tensor
+
+
+class MoELayer:
+    """Expert weights resident on the device plus reusable work buffers.
+
+    bf16 experts: ``w_gu`` [G,2I,H] (gate rows then up rows) and ``w_down``
+    [G,H,I].  int8 experts: ``q_gu``/``s_gu``/``q_down``/``s_down`` from
+    ``binding.moe_quantize_w8``.  G = E + S; the last S groups are shared
+    experts that every token visits with weight 1.
+    """
+
+    def __init__(self, H, E, k, I, S=0, renormalize=False, w_gu=None, w_down=None,
+                 q_gu=None, s_gu=None, q_down=None, s_down=None, device="cuda"):
+        self.H, self.E, self.k, self.I, self.S = H, E, k, I, S
+        self.G = E + S
+        self.renormalize = bool(renormalize)
+        self.device = torch.device(device)
+        self.int8 = q_gu is not None
+        if self.int8:
+            self.q_gu, self.s_gu, self.q_down, self.s_down = q_gu, s_gu, q_down, s_down
+        else:
+            if w_gu is None or w_down is None:
+                raise ValueError("bf16 weights or int8 weights are required")
+            self.w_gu, self.w_down = w_gu, w_down
+        self.err = B.new_error_word(self.device)
+        self._bufs: dict[int, LayerBuffers] = {}
+
+    def rows(self, T: int) -> int:
+        return T * self.k + self.S * T
+
+    def buffers(self, T: int) -> LayerBuffers:
+        b = self._bufs.get(T)
+        if b is None:
+            d = self.device
+            M = self.rows(T)
+            ws = B.moe_ffn_workspace_size(M, self.I)
+            b = LayerBuffers(
+                T=T,
+                topk_ids=torch.empty((T, self.k), dtype=torch.int32, device=d),
+                topk_w=torch.empty((T, self.k), dtype=torch.float32, device=d),
+                offsets=torch.empty(self.G + 1, dtype=torch.int32, device=d),
+                sorted_slot=torch.empty(T * self.k, dtype=torch.int32, device=d),
+                row_of_slot=torch.empty(T * self.k, dtype=torch.int32, device=d),
+                x_perm=torch.empty((M, self.H), dtype=torch.bfloat16, device=d),
+                y_perm=torch.empty((M, self.H), dtype=torch.bfloat16, device=d),
+                ffn_ws=torch.empty(max(ws, 256), dtype=torch.uint8, device=d),
+                out=torch.empty((T, self.H), dtype=torch.bfloat16, device=d),
+            )
+            self._bufs[T] = b
+        return b
+
+    def choose_ffn(self, T: int) -> str:
+        return "gemv" if self.rows(T) / self.G <= GEMV_MAX_ROWS_PER_GROUP else "gemm"
+
+    def route(self, logits, b: LayerBuffers, stream=None):
+        B.moe_route(logits, self.k, self.renormalize, b.topk_ids, b.topk_w, self.err, stream)
+
+    def permute(self, x, b: LayerBuffers, stream=None):
+        B.moe_permute(b.topk_ids, self.E, self.S, x, b.offsets, b.sorted_slot, b.row_of_slot,
+                      b.x_perm, None, self.err, stream)
+
+    def ffn(self, b: LayerBuffers, kind: str, stream=None):
+        if self.int8:
+            fn = B.moe_grouped_gemv_w8 if kind == "gemv" else B.moe_grouped_gemm_swiglu_w8
+            fn(b.x_perm, b.offsets, self.q_gu, self.s_gu, self.q_down, self.s_down, b.y_perm,
+               b.ffn_ws, self.err, stream)
+        else:
+            fn = B.moe_grouped_gemv if kind == "gemv" else B.moe_grouped_gemm_swiglu
+            fn(b.x_perm, b.offsets, self.w_gu, self.w_down, b.y_perm, b.ffn_ws, self.err, stream)
+
+    def combine(self, b: LayerBuffers, out, residual=None, stream=None):
+        B.moe_combine(b.y_perm, b.row_of_slot, b.topk_w, self.S, out, residual, self.err, stream)
+
+    def forward(self, x, logits, out=None, residual=None, ffn="auto", stream=None):
+        """out[t] = sum_j w[t,j] FFN_{id[t,j]}(x[t]) + sum_s FFN_{E+s}(x[t]) (+ residual[t])."""
+        T = x.shape[0]
+        b = self.buffers(T)
+        kind = self.choose_ffn(T) if ffn == "auto" else ffn
+        self.route(logits, b, stream)
+        self.permute(x, b, stream)
+        self.ffn(b, kind, stream)
+        dst = b.out if out is None else out
+        self.combine(b, dst, residual, stream)
+        return dst
+
+    def check(self):
+        """Synchronise and raise if any kernel reported a device-side fault."""
+        B.check_device_error(self.err, "MoELayer")
+
+
+class MoEStack:
+    """L MoE blocks with residual adds, x_{l+1} = bf16(x_l + MoE_l(x_l)); the
+    router logits of block l come from x_l on the device."""
+
+    def __init__(self, layers: list[MoELayer], routers: list[torch.Tensor], bias=None):
+        self.layers = layers
+        self.routers = routers
+        self.bias = bias
+        self._logits: dict[int, torch.Tensor] = {}
+        self._x: dict[int, tuple[torch.Tensor, torch.Tensor]] = {}
+
+    def forward(self, x, ffn="auto", stream=None, keep=None):
+        """Runs all blocks; returns the final activations (a reused buffer).
+        keep: optional list that receives (x_l, logits_l) clones per block."""
+        T = x.shape[0]
+        E = self.layers[0].E
+        L = self._logits.get(T)
+        if L is None:
+            L = self._logits[T] = torch.empty((T, E), dtype=torch.float32, device=x.device)
+        pair = self._x.get(T)
+        if pair is None:
+            pair = self._x[T] = (torch.empty_like(x), torch.empty_like(x))
+        cur = x
+        for i, (layer, w_r) in enumerate(zip(self.layers, self.routers)):
+            B.moe_router_logits(cur, w_r, self.bias, L, stream)
+            if keep is not None:
+                keep.append((cur.clone(), L.clone()))
+            nxt = pair[i % 2]
+            layer.forward(cur, L, out=nxt, residual=cur, ffn=ffn, stream=stream)
+            cur = nxt
+        return cur

@@ -1,0 +1,210 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the MoE token-dispatch hot path on one GB300
+ * (sm_103a).
+ *
+ * The layer these calls make up is the one the pages describe: route each
+ * token to its top-k experts, sort the token rows by expert, run every
+ * expert's SwiGLU FFN in one grouped launch, and combine the expert outputs
+ * back into token order ("switchyard" page, 02 Kernels and dispatch: "Route
+ * and sort", "One launch for all experts"; "dispatch" README, Architecture
+ * and Stack).  One layer is
+ *
+ *   moe_route -> moe_permute -> moe_grouped_gemm_swiglu | moe_grouped_gemv
+ *             -> moe_combine
+ *
+ * (int8 weight-only experts: the *_w8 calls, weights from moe_quantize_w8;
+ * a stack of layers takes its router logits from moe_router_logits).
+ *
+ * Conventions shared by every call
+ *  - Notation: T tokens, H hidden size, E routed experts, S shared experts
+ *    (always-on, weight 1), k experts per token, I expert intermediate size,
+ *    G = E + S expert groups, M = T*k + S*T permuted rows.  Slot s = t*k + j
+ *    is token t's j-th routed choice.
+ *  - Pointers are plain device pointers unless a parameter says "host".
+ *    The caller owns every buffer: the library never allocates device
+ *    memory, never synchronises, and enqueues all device work on `stream`
+ *    (asynchronous to the host).  bf16 tensors are passed as uint16_t bit
+ *    patterns.  All matrices are row-major and dense (no strides).
+ *  - Every device pointer must be 16-byte aligned; H and I must be
+ *    multiples of 8.  Otherwise MOE_ERR_ALIGNMENT.
+ *  - Limits: 1 <= T, 1 <= k <= min(E, 32), G <= 1024, T*k < 2^31, M*H < 2^31
+ *    elements.  Otherwise MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED.
+ *  - The return value reports what the host can see: argument checks and
+ *    launch errors (cudaGetLastError -> MOE_ERR_CUDA).  Faults in the data
+ *    (an expert id outside [0,E), a NaN logit, inconsistent offsets) are
+ *    found on the device: the kernel skips the offending write and stores
+ *    MOE_ERR_DEVICE_CHECK into *dev_error; a bounded wait that ran out
+ *    stores MOE_ERR_TIMEOUT.  dev_error is one int32 in device memory that
+ *    the caller zeroes and reads after synchronising; it may be NULL, in
+ *    which case device-side faults are not reported (writes are still
+ *    skipped).
+ *  - Results are deterministic: the same inputs give the same bytes on
+ *    every run (no atomics on any data path).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, k > E ... */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but outside this build's limits */
+    MOE_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned, H or I not a multiple of 8 */
+    MOE_ERR_WORKSPACE = 4,     /* workspace smaller than the *_workspace_size answer */
+    MOE_ERR_CUDA = 5,          /* a CUDA runtime / driver call failed */
+    MOE_ERR_DEVICE_CHECK = 6,  /* device-side data check failed (see dev_error) */
+    MOE_ERR_TIMEOUT = 7        /* a bounded device-side wait ran out (see dev_error) */
+} moe_status;
+
+typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
+
+/* Static description of a status code; never NULL. */
+const char *moe_status_string(int status);
+
+/* Library version as an integer (major*10000 + minor*100 + patch). */
+int moe_version(void);
+
+/*
+ * moe_router_logits -- router logits of a bf16 activation batch.
+ * logits[t,e] = sum_c x[t,c] * w_r[e,c] (+ bias[e]), fp32 accumulation in a
+ * fixed order.  The pages leave the router as plain PyTorch ("dispatch"
+ * README, Architecture: "Router / top-k gating"); this call exists so a
+ * stack of layers (x_{l+1} = x_l + MoE_l(x_l)) can route layer l+1 on the
+ * device.  x: [T,H] bf16; w_r: [E,H] bf16 (one row per expert); bias: [E]
+ * fp32 or NULL (a fixed routing bias, e.g. a zipf skew); logits: [T,E] fp32.
+ */
+moe_status moe_router_logits(const uint16_t *x, const uint16_t *w_r, const float *bias, int T,
+                             int H, int E, float *logits, cudaStream_t stream);
+
+/*
+ * moe_route -- top-k routing, one warp per token ("switchyard" page, "Route
+ * and sort": each token routed in one warp).
+ * logits: [T,E] fp32.  topk_ids: [T,k] int32, the k experts with the
+ * largest logit in descending order, ties broken toward the lower expert
+ * index.  topk_w: [T,k] fp32, softmax over all E logits of each chosen
+ * expert; if `renormalize` is non-zero the k weights are divided by their
+ * sum.  A NaN logit is a device-check fault (that token's outputs are
+ * left untouched).  E <= 1024.
+ */
+moe_status moe_route(const float *logits, int T, int E, int k, int renormalize,
+                     int32_t *topk_ids, float *topk_w, int32_t *dev_error, cudaStream_t stream);
+
+/* Workspace bytes moe_permute needs (currently 0: it works in shared memory). */
+size_t moe_permute_workspace_size(int T, int E, int S, int k);
+
+/*
+ * moe_permute -- stable sort of token rows by expert with a block-wide
+ * prefix scan and no atomics ("switchyard" page, "Route and sort"), plus
+ * the gather of activation rows into expert order.
+ * topk_ids: [T,k] int32 from moe_route.  x: [T,H], bf16 (x_dtype =
+ * MOE_DTYPE_BF16) or fp32 (MOE_DTYPE_F32, rounded to bf16 on the gather).
+ * Outputs:
+ *   offsets     [G+1] int32: group g owns permuted rows [offsets[g],
+ *               offsets[g+1]); routed group e holds its slots in ascending
+ *               slot order; shared group E+s holds tokens 0..T-1 in order;
+ *               offsets[0] = 0, offsets[E] = T*k, offsets[G] = M.
+ *   sorted_slot [T*k] int32: the slot held by routed row r.
+ *   row_of_slot [T*k] int32: inverse of sorted_slot (-1 for a slot whose
+ *               expert id was invalid).
+ *   x_perm      [M,H] bf16: row r = x[token of row r].
+ * An expert id outside [0,E) is a device-check fault; that slot is dropped.
+ */
+moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, int k, const void *x,
+                       int x_dtype, int H, int32_t *offsets, int32_t *sorted_slot,
+                       int32_t *row_of_slot, uint16_t *x_perm, void *workspace,
+                       size_t workspace_bytes, int32_t *dev_error, cudaStream_t stream);
+
+/* Workspace bytes of the FFN calls below: the bf16 hidden rows h [M,I]. */
+size_t moe_ffn_workspace_size(int M, int I);
+
+/*
+ * moe_grouped_gemm_swiglu -- every expert's SwiGLU FFN over its permuted
+ * rows in one persistent launch per GEMM ("switchyard" page, "One launch
+ * for all experts": a tensor-core grouped GEMM with SwiGLU fused into its
+ * epilogue).  tcgen05 MMAs with TMEM accumulators fed by TMA, a per-expert
+ * tile scheduler over the offsets table.
+ *   h[r,:]      = bf16( silu(x_perm[r] . Wg_g^T) * (x_perm[r] . Wu_g^T) )
+ *   y_perm[r,:] = bf16( h[r] . Wd_g^T )          for rows r of group g
+ * x_perm: [M,H] bf16; offsets: [G+1] from moe_permute (read on the device:
+ * the host never needs the per-expert counts); w_gu: [G,2I,H] bf16, rows
+ * 0..I-1 of each group the gate projection, rows I..2I-1 the up projection;
+ * w_down: [G,H,I] bf16; y_perm: [M,H] bf16 (unweighted: the routing weight
+ * is applied by moe_combine).  workspace: at least
+ * moe_ffn_workspace_size(M, I) bytes of device memory (holds h).
+ * Offsets that are not monotone or exceed M are a device-check fault (no
+ * output is written).  Rows beyond offsets[G] are not touched.
+ */
+moe_status moe_grouped_gemm_swiglu(const uint16_t *x_perm, const int32_t *offsets, int G, int M,
+                                   int H, int I, const uint16_t *w_gu, const uint16_t *w_down,
+                                   uint16_t *y_perm, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * moe_grouped_gemv -- the same computation as moe_grouped_gemm_swiglu for
+ * decode-sized batches: each expert weight row is streamed from HBM once
+ * with coalesced 128-bit loads and dotted with the few rows of its expert
+ * ("switchyard" page, "One launch for all experts": for decode, a grouped
+ * GEMV).  Same arguments and results (up to fp32 summation order).  Fast
+ * when the mean rows per expert is small (about <= 4); correct for any.
+ */
+moe_status moe_grouped_gemv(const uint16_t *x_perm, const int32_t *offsets, int G, int M, int H,
+                            int I, const uint16_t *w_gu, const uint16_t *w_down,
+                            uint16_t *y_perm, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * int8 weight-only variants ("dispatch" README, phase 5a: per-channel int8
+ * weight-only quantisation).  q_gu: [G,2I,H] int8 with s_gu: [G,2I] fp32
+ * (one scale per output row); q_down: [G,H,I] int8 with s_down: [G,H].
+ * The effective weight is (float)q * scale; the kernels accumulate
+ * sum x*q in fp32 and multiply by the row's scale.  Otherwise as above.
+ */
+moe_status moe_grouped_gemm_swiglu_w8(const uint16_t *x_perm, const int32_t *offsets, int G,
+                                      int M, int H, int I, const int8_t *q_gu, const float *s_gu,
+                                      const int8_t *q_down, const float *s_down,
+                                      uint16_t *y_perm, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_error, cudaStream_t stream);
+moe_status moe_grouped_gemv_w8(const uint16_t *x_perm, const int32_t *offsets, int G, int M,
+                               int H, int I, const int8_t *q_gu, const float *s_gu,
+                               const int8_t *q_down, const float *s_down, uint16_t *y_perm,
+                               void *workspace, size_t workspace_bytes, int32_t *dev_error,
+                               cudaStream_t stream);
+
+/*
+ * moe_combine -- weighted sum of each token's expert rows back in token
+ * order, by gathering (no scatter-add, so the result is the same bytes on
+ * every run; the "Phase 6" pull request of "dispatch", Summary, reports
+ * the atomic index_add_ combine as not bitwise deterministic).
+ *   out[t] = bf16( sum_{j<k} topk_w[t,j] * y_perm[row_of_slot[t*k+j]]
+ *                  + sum_{s<S} y_perm[T*k + s*T + t]  (+ residual[t]) )
+ * summed in fp32 in that order.  y_perm: [M,H] bf16; row_of_slot: [T*k];
+ * topk_w: [T,k] fp32; residual: [T,H] bf16 or NULL; out: [T,H] bf16 (may
+ * alias residual).  A row index outside [0, T*k) is skipped.
+ */
+moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_slot, const float *topk_w,
+                       int T, int k, int S, int H, const uint16_t *residual, uint16_t *out,
+                       int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * moe_quantize_w8 -- offline, host-side int8 quantisation of expert
+ * weights ("dispatch" README, phase 5a: self-computed per-channel scales).
+ * w_host: [rows, K] bf16 bits in host memory; q_host: [rows, K] int8 and
+ * scale_host: [rows] fp32, host memory.  Per row: scale = max|w| / 127 in
+ * fp32 (1 for an all-zero row); q = clamp(round-half-even(w / scale),
+ * -127, 127), the quotient taken in fp32.  Synchronous; no device work.
+ */
+moe_status moe_quantize_w8(const uint16_t *w_host, int64_t rows, int64_t K, int8_t *q_host,
+                           float *scale_host);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,280 @@
+"""CUDA path vs the CPU oracle on seeded inputs, through the C-ABI calls.
+
+Bars: routing ids, permutation and offsets bit-exact (given the same fp32
+logits); routing weights within 1e-6 relative; bf16 layer outputs within
+relative Frobenius error 5e-3 and max |diff| <= 2e-2 * max|ref| of the
+oracle's exact layer; the same bytes on every run.  Shapes are the pages'
+OLMoE-1B-7B and DeepSeek-MoE-16B layers ("switchyard" page intro;
+"dispatch" README, Stack) plus small shapes that span several tiles with
+ragged tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from grouped_expert_gemm_moe_gb300 import workloads as W
+
+from gpu_helpers import (W_RTOL, assert_close, errors, host_inputs, oracle_out, sample_tokens,
+                         to_np)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__ as g
+    g.build()
+    from grouped_expert_gemm_moe_gb300 import binding
+    return binding
+
+
+@pytest.fixture(scope="module")
+def L(B):
+    from grouped_expert_gemm_moe_gb300 import layer
+    return layer
+
+
+_CACHE = {}
+
+
+def layer_case(name, T, routing):
+    key = (name, T, routing)
+    if key not in _CACHE:
+        _CACHE.clear()                                     # keep one full-size layer resident
+        sh = W.CONFIGS[name]
+        big = sh.H * sh.I * sh.G > 10_000_000
+        inp = W.make_layer(sh, T, routing, seed=0, device=DEV if big else "cpu")
+        _CACHE[key] = (inp, host_inputs(inp))
+    return _CACHE[key]
+
+
+def make_layer_obj(L, inp):
+    sh = inp.shape
+    return L.MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize,
+                      w_gu=inp.w_gu.to(DEV), w_down=inp.w_down.to(DEV), device=DEV)
+
+
+CASES = [("tiny", 16, "uniform"),
+         ("olmoe", 1, "uniform"), ("olmoe", 8, "uniform"), ("olmoe", 64, "uniform"),
+         ("deepseek", 1, "uniform"), ("deepseek", 16, "zipf"), ("deepseek", 128, "uniform"),
+         ("deepseek", 512, "zipf"), ("deepseek", 2048, "uniform"), ("deepseek", 2048, "zipf")]
+
+
+@pytest.mark.parametrize("name,T,routing", CASES)
+def test_route_and_permute_bit_exact(B, L, name, T, routing):
+    inp, h = layer_case(name, T, routing)
+    sh = inp.shape
+    layer = make_layer_obj(L, inp)
+    b = layer.buffers(T)
+    x, logits = inp.x.to(DEV), inp.logits.to(DEV)
+    layer.route(logits, b)
+    layer.permute(x, b)
+    layer.check()
+    ids_ref, w_ref = oracle.route(h["logits"], sh.k, sh.renormalize)
+    np.testing.assert_array_equal(b.topk_ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(b.topk_w.cpu().numpy().astype(np.float64), w_ref, rtol=W_RTOL)
+    off, ss, ros = oracle.permute(ids_ref, sh.E, sh.S)
+    np.testing.assert_array_equal(b.offsets.cpu().numpy(), off)
+    np.testing.assert_array_equal(b.sorted_slot.cpu().numpy(), ss)
+    np.testing.assert_array_equal(b.row_of_slot.cpu().numpy(), ros)
+    # x_perm rows are the tokens' rows (rounded to bf16 for fp32 activations)
+    tok = np.concatenate([ss // sh.k] + [np.arange(T)] * sh.S)
+    xb = inp.x.to(torch.bfloat16).cpu()
+    assert torch.equal(b.x_perm.cpu(), xb[torch.from_numpy(tok).long()])
+
+
+@pytest.mark.parametrize("ffn", ["gemm", "gemv"])
+@pytest.mark.parametrize("name,T,routing", CASES)
+def test_layer_matches_oracle(B, L, name, T, routing, ffn):
+    if ffn == "gemv" and T > 512:
+        pytest.skip("the GEMV is for decode-sized batches")
+    inp, h = layer_case(name, T, routing)
+    layer = make_layer_obj(L, inp)
+    out = layer.forward(inp.x.to(DEV), inp.logits.to(DEV), ffn=ffn)
+    layer.check()
+    tok = sample_tokens(T)
+    _, _, y = oracle_out(inp, h, tokens=tok)
+    rel, mx = assert_close(to_np(out)[tok], y, f"{name} T={T} {routing} {ffn}")
+    print(f"{name} T={T} {routing} {ffn}: rel {rel:.2e} max {mx:.2e}")
+
+
+def test_gemm_and_gemv_agree_and_are_deterministic(B, L):
+    inp, h = layer_case("deepseek", 128, "uniform")
+    layer = make_layer_obj(L, inp)
+    x, logits = inp.x.to(DEV), inp.logits.to(DEV)
+    outs = {}
+    for ffn in ("gemm", "gemv"):
+        runs = [layer.forward(x, logits, ffn=ffn).clone() for _ in range(3)]
+        layer.check()
+        for r in runs[1:]:
+            assert torch.equal(r, runs[0]), f"{ffn} output changed between runs"
+        outs[ffn] = to_np(runs[0])
+    rel, mx = errors(outs["gemm"], outs["gemv"])
+    assert rel < 5e-3 and mx < 2e-2
+
+
+def _ffn_rows_oracle(xp_bits, off, w_gu_bits, w_down_bits, H, I):
+    """Per permuted row: y = FFN_g(x_perm[r]) (unweighted), oracle fp64."""
+    M = xp_bits.shape[0]
+    y = np.zeros((M, H))
+    xv = (xp_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for g in range(len(off) - 1):
+        for r in range(off[g], off[g + 1]):
+            hh = oracle.expert_hidden(xv[r], w_gu_bits[g], H, I)
+            y[r] = oracle.expert_down(hh, w_down_bits[g], H, I)
+    return y
+
+
+@pytest.mark.parametrize("ffn", ["gemm", "gemv"])
+@pytest.mark.parametrize("H,I,E,S,k,T", [(136, 200, 5, 1, 2, 300),     # K and N tails
+                                          (256, 512, 4, 0, 1, 1000),   # several m-tiles + tail
+                                          (512, 384, 16, 2, 4, 97)])
+def test_grouped_ffn_rows_vs_oracle(B, L, ffn, H, I, E, S, k, T):
+    """The grouped FFN alone: every permuted row against the oracle's expert
+    FFN, on shapes whose tiles have ragged M, N and K tails."""
+    sh = W.MoEShape("t", H=H, E=E, k=k, I=I, S=S)
+    inp = W.make_layer(sh, T, "uniform", seed=1)
+    layer = make_layer_obj(L, inp)
+    b = layer.buffers(T)
+    layer.route(inp.logits.to(DEV), b)
+    layer.permute(inp.x.to(DEV), b)
+    layer.ffn(b, ffn)
+    layer.check()
+    off = b.offsets.cpu().numpy()
+    ref = _ffn_rows_oracle(W.bf16_bits(b.x_perm), off, W.bf16_bits(inp.w_gu),
+                           W.bf16_bits(inp.w_down), H, I)
+    got = to_np(b.y_perm)
+    M = layer.rows(T)
+    rel, mx = errors(got[:M], ref[:M])
+    if not (rel <= 5e-3 and mx <= 2e-2):
+        bad = np.abs(got - ref) > 2e-2 * np.abs(ref).max()
+        rows = np.where(bad.any(1))[0]
+        cols = np.where(bad.any(0))[0]
+        pytest.fail(f"{ffn}: rel {rel:.3e} max {mx:.3e}; bad rows {rows[:20]}.. "
+                    f"({len(rows)}), bad cols {cols[:20]}.. ({len(cols)})")
+
+
+def _adversarial_logits(kind, T, E):
+    if kind == "all_to_one":
+        L = np.full((T, E), -3.0, np.float32)
+        L[:, 5] = 4.0
+        return L
+    if kind == "ties":
+        rng = np.random.default_rng(0)
+        return rng.integers(0, 3, size=(T, E)).astype(np.float32)
+    if kind == "equal":
+        return np.zeros((T, E), np.float32)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["all_to_one", "ties", "equal"])
+@pytest.mark.parametrize("ffn", ["gemm", "gemv"])
+def test_adversarial_routings(B, L, kind, ffn):
+    sh = W.MoEShape("adv", H=256, E=16, k=4, I=256, S=1, renormalize=True)
+    T = 300
+    inp = W.make_layer(sh, T, "uniform", seed=2)
+    inp.logits = torch.from_numpy(_adversarial_logits(kind, T, sh.E))
+    h = host_inputs(inp)
+    layer = make_layer_obj(L, inp)
+    out = layer.forward(inp.x.to(DEV), inp.logits.to(DEV), ffn=ffn)
+    layer.check()
+    ids, w, y = oracle_out(inp, h)
+    b = layer.buffers(T)
+    np.testing.assert_array_equal(b.topk_ids.cpu().numpy(), ids)
+    np.testing.assert_array_equal(b.offsets.cpu().numpy(), oracle.permute(ids, sh.E, sh.S)[0])
+    assert_close(to_np(out), y, f"{kind} {ffn}")
+
+
+def test_single_token_single_expert(B, L):
+    sh = W.MoEShape("one", H=64, E=1, k=1, I=64)
+    inp = W.make_layer(sh, 1, "uniform", seed=3)
+    h = host_inputs(inp)
+    layer = make_layer_obj(L, inp)
+    for ffn in ("gemm", "gemv"):
+        out = layer.forward(inp.x.to(DEV), inp.logits.to(DEV), ffn=ffn)
+        layer.check()
+        _, _, y = oracle_out(inp, h)
+        assert_close(to_np(out), y, f"T=1 E=1 {ffn}")
+
+
+def test_residual_and_aliasing(B, L):
+    inp, h = layer_case("tiny", 16, "uniform")
+    sh = inp.shape
+    layer = make_layer_obj(L, inp)
+    res = (torch.randn((16, sh.H), generator=torch.Generator().manual_seed(9))).to(torch.bfloat16)
+    buf = res.to(DEV).clone()
+    layer.forward(inp.x.to(DEV), inp.logits.to(DEV), out=buf, residual=buf, ffn="gemm")
+    layer.check()
+    _, _, y = oracle_out(inp, h, residual=W.bf16_bits(res))
+    assert_close(to_np(buf), y, "residual")
+
+
+def test_invalid_expert_id_is_reported_without_out_of_bounds(B, L):
+    sh = W.MoEShape("bad", H=64, E=8, k=2, I=64, S=1)
+    T = 10
+    inp = W.make_layer(sh, T, "uniform", seed=4)
+    layer = make_layer_obj(L, inp)
+    b = layer.buffers(T)
+    ids = torch.randint(0, sh.E, (T, sh.k), dtype=torch.int32)
+    ids[3, 1] = sh.E                        # out of range
+    b.topk_ids.copy_(ids)
+    b.topk_w.fill_(0.5)
+    b.y_perm.zero_()
+    layer.permute(inp.x.to(DEV), b)
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 6
+    assert (b.offsets.cpu() == 0).all() and (b.row_of_slot.cpu() == -1).all()
+    layer.err.zero_()
+    for ffn in ("gemm", "gemv"):
+        layer.ffn(b, ffn)                   # empty groups: no work, no error
+    out = torch.empty((T, sh.H), dtype=torch.bfloat16, device=DEV)
+    layer.combine(b, out)
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 6       # combine skipped the unplaced slots
+
+
+def test_nan_logit_is_reported(B, L):
+    inp, _ = layer_case("tiny", 16, "uniform")
+    layer = make_layer_obj(L, inp)
+    b = layer.buffers(16)
+    logits = inp.logits.clone()
+    logits[2, 3] = float("nan")
+    layer.route(logits.to(DEV), b)
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 6
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_w8_gemv_matches_oracle(B, L, T):
+    sh = W.OLMOE
+    inp = W.make_layer(sh, T, "uniform", seed=0, device=DEV)
+    h = host_inputs(inp)
+    q_gu, s_gu = B.moe_quantize_w8(inp.w_gu)
+    q_down, s_down = B.moe_quantize_w8(inp.w_down)
+    layer = L.MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize, q_gu=q_gu.to(DEV),
+                       s_gu=s_gu.to(DEV), q_down=q_down.to(DEV), s_down=s_down.to(DEV),
+                       device=DEV)
+    out = layer.forward(inp.x, inp.logits, ffn="gemv")
+    layer.check()
+    tok = sample_tokens(T)
+    ids, w = oracle.route(h["logits"], sh.k, sh.renormalize)
+    y = oracle.moe_layer_w8(h["x"], ids, w, sh.E, sh.S, q_gu.numpy(), s_gu.numpy(),
+                            q_down.numpy(), s_down.numpy(), tokens=tok)
+    assert_close(to_np(out)[tok], y, f"w8 gemv T={T}")
+
+
+def test_router_logits_kernel(B):
+    sh = W.OLMOE
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn((77, sh.H), generator=g).to(torch.bfloat16)
+    w_r = (torch.randn((sh.E, sh.H), generator=g) * 0.02).to(torch.bfloat16)
+    bias = W.zipf_bias(sh.E, 0.5)
+    out = torch.empty((77, sh.E), dtype=torch.float32, device=DEV)
+    B.moe_router_logits(x.to(DEV), w_r.to(DEV), bias.to(DEV), out)
+    ref = oracle.router_logits(W.bf16_bits(x), W.bf16_bits(w_r), bias.numpy())
+    got = out.cpu().numpy().astype(np.float64)
+    # fp32 accumulation of 2048 products: error << 1e-4 of the logit scale
+    assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
