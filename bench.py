@@ -1,0 +1,576 @@
+#!/usr/bin/env python3
+"""MoE-layer throughput of the token-dispatch hot path on GB300.
+
+One step = one pass of the whole layer over one batch: route -> permute ->
+grouped FFN (gate/up + SwiGLU, then down) -> combine, every kernel this
+library's.  Default workload: the OLMoE-shaped decode layer (hidden 2048,
+64 experts, top-8, intermediate 1024, bf16) at T=64 tokens, with T=1 and
+T=8 reported beside it.  Inputs are seeded synthetic tensors; expert
+weights (805 MB) exceed the 129 MB L2 and L2 is flushed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Prints one JSON line (rank 0).  With --gpus N > 1 (launched by torchrun)
+every rank runs an independent replica on its own batch (the layer has no
+cross-GPU exchange on one GPU per expert set), value = all tokens / max
+rank time.  --impl reference times the CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and µs/layer at T=1..2048; % of HBM BW (decode) / tensor peak"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+# name -> (shape config, T, routing, extra T values measured beside it)
+WORKLOADS = {
+    "olmoe_decode_t64": ("olmoe", 64, "uniform", (1, 8)),
+    "olmoe_decode_t8": ("olmoe", 8, "uniform", ()),
+    "olmoe_decode_t1": ("olmoe", 1, "uniform", ()),
+    "olmoe_t2048": ("olmoe", 2048, "uniform", (128, 512)),
+    "deepseek_t2048": ("deepseek", 2048, "uniform", (1, 16, 128, 512)),
+    "deepseek_t2048_zipf": ("deepseek", 2048, "zipf", (1, 16, 128, 512)),
+}
+DEFAULT_WORKLOAD = "olmoe_decode_t64"
+
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity at world size 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_value(tokens_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job tokens/s: tokens of every rank over the slowest rank's time."""
+    return tokens_per_rank * world / max_seconds
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained",
+                                                      p["bf16_tflops"])), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "gemv.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "grouped_expert_gemm_moe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[f"{kernel}@{workload}"]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 100 ms; stop(t0, t1)
+    keeps the samples taken inside the wall-clock window [t0, t1]."""
+
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        import tempfile
+        self.proc = None
+        self.fh = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    @staticmethod
+    def _ts(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.fh.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.remove(self.fh.name)
+        inside = [r for r in rows if (ts := self._ts(r[0])) is not None and t0 <= ts <= t1]
+        use = inside if inside else rows
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for r in use if (v := num(r[2])) is not None]
+        mx = [v for r in use if (v := num(r[3])) is not None]
+        reasons = sorted({self.REASONS[i] for r in use for i in range(4)
+                          if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------ workload
+
+def build_workload(name, device, seed):
+    from grouped_expert_gemm_moe_gb300 import workloads as W
+    from grouped_expert_gemm_moe_gb300.layer import MoELayer
+    cfg, T, routing, extra = WORKLOADS[name]
+    shape = W.CONFIGS[cfg]
+    inp = W.make_layer(shape, T, routing, seed=seed, device=device)
+    layer = MoELayer(shape.H, shape.E, shape.k, shape.I, shape.S, shape.renormalize,
+                     w_gu=inp.w_gu, w_down=inp.w_down, device=device)
+    return shape, T, routing, extra, inp, layer
+
+
+def extra_batch(shape, T, routing, seed, device, inp):
+    """Another batch (x, logits) for the same layer weights."""
+    import torch
+    from grouped_expert_gemm_moe_gb300 import workloads as W
+    g = W.make_generator(seed + 7919 * T, device)
+    x = torch.randn((T, shape.H), generator=g, device=device).to(torch.bfloat16)
+    return x, W.router_logits_input(x, inp.w_r, inp.bias)
+
+
+class Phases:
+    """One layer step recorded as three CUDA graphs -- [route, permute],
+    [gate/up], [down, combine] -- so the dominant kernel can be timed with
+    events between graph launches inside the timed region."""
+
+    def __init__(self, layer, x, logits, kind):
+        import torch
+        self.layer, self.kind = layer, kind
+        b = self.b = layer.buffers(x.shape[0])
+
+        def pre():
+            layer.route(logits, b)
+            layer.permute(x, b)
+
+        def mid():
+            layer.gate_up(b, kind)
+
+        def post():
+            layer.down(b, kind)
+            layer.combine(b, b.out)
+
+        self.graphs = []
+        for fn in (pre, mid, post):
+            fn()                                   # eager pass: attributes set outside capture
+        torch.cuda.synchronize()
+        for fn in (pre, mid, post):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                fn()
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def run(self, ev=None):
+        g0, g1, g2 = self.graphs
+        if ev is None:
+            g0.replay(); g1.replay(); g2.replay()
+            return
+        s, k0, k1, e = ev
+        s.record()
+        g0.replay()
+        k0.record()
+        g1.replay()
+        k1.record()
+        g2.replay()
+        e.record()
+
+
+KERNELS_PER_STEP = 6      # route, permute index, permute gather, gate/up, down, combine
+
+
+def touched_groups(layer, b):
+    import numpy as np
+    off = b.offsets.cpu().numpy()
+    return int(np.count_nonzero(np.diff(off) > 0))
+
+
+def time_steps(phases, K, W, flush):
+    """W warm-up steps, then K timed steps, L2 flushed before each step.
+    Returns per-step and per-gate/up-launch device times (ms)."""
+    import torch
+    for _ in range(W):
+        flush.zero_()
+        phases.run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        phases.run(evs[i])
+    torch.cuda.synchronize()
+    step = [e[0].elapsed_time(e[3]) for e in evs]
+    gate_up = [e[1].elapsed_time(e[2]) for e in evs]
+    return step, gate_up
+
+
+def layer_roofline(shape, T, n_groups, peaks):
+    """Ideal layer time: max(FLOPs / bf16 peak, algorithmic bytes / HBM BW).
+    Bytes: weights of served groups (3*H*I*2) + x in + out (T*H*2 each);
+    FLOPs: 6*H*I per served row (routed slots + shared rows)."""
+    H, I = shape.H, shape.I
+    bytes_ = n_groups * 3 * H * I * 2 + 2 * T * H * 2
+    flops = 6.0 * H * I * shape.rows(T)
+    t_mem = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_flop = flops / (peaks["bf16_tflops"] * 1e12)
+    return dict(bytes=bytes_, flops=flops, t_roof_us=max(t_mem, t_flop) * 1e6,
+                bound="hbm" if t_mem >= t_flop else "tensor")
+
+
+def kernel_roofline(shape, T, n_groups, gate_up_ms, peaks, kind, workload):
+    """Roofline of the gate/up kernel: its algorithmic bytes are the gate and
+    up weights of the served groups (2*I*H*2 per group); its FLOPs are
+    4*H*I per served row."""
+    H, I = shape.H, shape.I
+    bytes_ = n_groups * 2 * I * H * 2
+    flops = 4.0 * H * I * shape.rows(T)
+    sec = gate_up_ms / 1e3
+    t_mem = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_flop = flops / (peaks["bf16_tflops"] * 1e12)
+    name = "tc_grouped_gemm_swiglu" if kind == "gemm" else "gemv_gateup_bf16"
+    traffic = profiled_traffic(name, workload)
+    if t_mem >= t_flop:
+        ach = bytes_ / sec / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes": bytes_,
+                "avg_launch_us": round(gate_up_ms * 1e3, 2),
+                "peak_source": f"{peaks['source']} (STREAM copy, burst)"}
+    ach = flops / sec / 1e12
+    return {"kernel": name, "bound": "tensor", "achieved": round(ach, 1),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
+            "algorithmic_flops": flops, "avg_launch_us": round(gate_up_ms * 1e3, 2),
+            "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
+
+
+def measure_T(layer, shape, T, x, logits, K, W, flush, peaks, workload):
+    kind = layer.choose_ffn(T)
+    ph = Phases(layer, x, logits, kind)
+    step, gu = time_steps(ph, K, W, flush)
+    n_groups = touched_groups(layer, ph.b)
+    ms = statistics.fmean(step)
+    roof = layer_roofline(shape, T, n_groups, peaks)
+    return dict(kind=kind, step_ms=step, gate_up_ms=statistics.fmean(gu), ms=ms,
+                n_groups=n_groups, roof=roof,
+                kroof=kernel_roofline(shape, T, n_groups, statistics.fmean(gu), peaks, kind,
+                                      workload))
+
+
+def e2e_measure(layer, shape, T, inp, K, W, flush):
+    """End to end through the public API: pinned host x and logits copied in,
+    the captured forward pass, the output copied back, every step."""
+    import torch
+    dev = layer.device
+    x_host = inp.x.detach().cpu().pin_memory()
+    l_host = inp.logits.detach().cpu().pin_memory()
+    out_host = torch.empty((T, shape.H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp.x, device=dev)
+    l_dev = torch.empty_like(inp.logits, device=dev)
+    x_dev.copy_(x_host)
+    l_dev.copy_(l_host)
+    cap = layer.capture(x_dev, l_dev)
+
+    def step():
+        x_dev.copy_(x_host, non_blocking=True)
+        l_dev.copy_(l_host, non_blocking=True)
+        out = cap.replay()
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(W):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record()
+        step()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+    h2d = x_host.numel() * x_host.element_size() + l_host.numel() * l_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
+    return ms, h2d, d2h, out_host.clone()
+
+
+# ------------------------------------------------------------ oracle legs
+
+def oracle_sample(inp, tokens):
+    """The oracle's view of the given tokens: fp32 logits and x (fp32, or
+    bf16 bit patterns)."""
+    import numpy as np
+    import torch
+
+    from grouped_expert_gemm_moe_gb300 import workloads as W
+    logits = inp.logits.detach().cpu().numpy()[tokens]
+    xb = inp.x.detach().cpu()
+    x = xb.numpy()[tokens] if xb.dtype == torch.float32 else W.bf16_bits(xb)[tokens]
+    return dict(logits=np.ascontiguousarray(logits), x=np.ascontiguousarray(x))
+
+
+def run_oracle_tokens(inp, host, tokens, wbits):
+    import oracle
+    sh = inp.shape
+    ids, w = oracle.route(host["logits"], sh.k, sh.renormalize)
+    oracle.permute(ids, sh.E, sh.S)
+    return oracle.moe_layer(host["x"], ids, w, sh.E, sh.S, wbits[0], wbits[1])
+
+
+def cpu_baseline(inp, gpu_out, max_tokens=64):
+    """The oracle, as it stands, on the host cores over (up to) the first
+    max_tokens tokens of the batch; also the parity gate of the bench: a
+    GPU result that disagrees with it is not timed."""
+    import numpy as np
+
+    import oracle
+    from grouped_expert_gemm_moe_gb300 import workloads as W
+    T = inp.T
+    tokens = np.arange(min(T, max_tokens))
+    host = oracle_sample(inp, tokens)
+    wbits = (W.bf16_bits(inp.w_gu), W.bf16_bits(inp.w_down))
+    t0 = time.perf_counter()
+    y = run_oracle_tokens(inp, host, tokens, wbits)
+    sec = time.perf_counter() - t0
+    got = gpu_out.float().cpu().numpy().astype(np.float64)[tokens]
+    rel = float(np.linalg.norm(got - y) / np.linalg.norm(y))
+    mx = float(np.abs(got - y).max() / np.abs(y).max())
+    cores = min(len(tokens), oracle.num_threads())
+    return dict(value=round(len(tokens) / sec, 3), unit=UNIT, cores=cores, kind="oracle",
+                sample=f"route+permute+layer of tokens 0..{len(tokens) - 1} of the timed batch "
+                       f"({len(tokens)} tokens, {sec:.2f} s)",
+                parity={"rel_frobenius": rel, "max_rel": mx, "ok": rel <= 5e-3 and mx <= 2e-2})
+
+
+# ------------------------------------------------------------------ arms
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    shape, T, routing, extra, inp, layer = build_workload(args.workload, dev, seed=rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # correctness first: one pass, checked against the oracle before timing
+    out0 = layer.forward(inp.x, inp.logits).clone()
+    layer.check()
+    base = None
+    if rank == 0 and world == 1:
+        base = cpu_baseline(inp, out0)
+        if not base["parity"]["ok"]:
+            print(json.dumps({"error": "GPU result disagrees with the oracle; not timed",
+                              "parity": base["parity"]}))
+            sys.exit(1)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.5)                         # let nvidia-smi start sampling
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    m = measure_T(layer, shape, T, inp.x, inp.logits, args.steps, args.warmup, flush, peaks,
+                  args.workload)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler is not None else None
+    layer.check()
+
+    sec = reduce_max(sum(m["step_ms"]) / 1e3, world, dev)
+    value = aggregate_value(T * args.steps, world, sec)
+    ms_per_step = sec * 1e3 / args.steps
+
+    per_T = {}
+    for t2 in extra:
+        x2, l2 = extra_batch(shape, t2, routing, rank, dev, inp)
+        m2 = measure_T(layer, shape, t2, x2, l2, args.steps, args.warmup, flush, peaks,
+                       args.workload)
+        per_T[str(t2)] = {"us_per_layer": round(m2["ms"] * 1e3, 2),
+                          "tokens_per_s": round(t2 / (m2["ms"] / 1e3), 1), "ffn": m2["kind"],
+                          "roofline_frac": round(m2["roof"]["t_roof_us"] / (m2["ms"] * 1e3), 4),
+                          "gate_up_frac": m2["kroof"]["frac"], "groups": m2["n_groups"]}
+    layer.check()
+
+    e2e_ms, h2d, d2h, out_e2e = e2e_measure(layer, shape, T, inp, args.steps, args.warmup, flush)
+    layer.check()
+    e2e_sec = reduce_max(e2e_ms * args.steps / 1e3, world, dev)
+    if not torch.equal(out_e2e.to(dev), out0):
+        print(json.dumps({"error": "end-to-end output differs from the first pass"}))
+        sys.exit(1)
+
+    if rank == 0:
+        roof = m["roof"]
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) bf16 expert weights)",
+            "impl": "ours",
+            "config": {"workload": args.workload, "layer": shape.name, "T": T,
+                       "H": shape.H, "E": shape.E, "k": shape.k, "I": shape.I, "S": shape.S,
+                       "routing": routing, "ffn": m["kind"], "served_groups": m["n_groups"],
+                       "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "timing": "CUDA events per step on the launch stream; step = 3 graph "
+                                 "launches [route+permute][gate/up][down+combine]"},
+            "us_per_layer": round(m["ms"] * 1e3, 2),
+            "layer_roofline": {"t_roof_us": round(roof["t_roof_us"], 2), "bound": roof["bound"],
+                               "frac": round(roof["t_roof_us"] / (m["ms"] * 1e3), 4),
+                               "algorithmic_bytes": roof["bytes"],
+                               "peak_source": peaks["source"]},
+            "roofline": m["kroof"],
+            "per_T": per_T,
+            "e2e": {"value": round(aggregate_value(T * args.steps, world, e2e_sec), 1),
+                    "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "us_per_step": round(e2e_ms * 1e3, 2),
+                    "path": "pinned host x+logits -> MoELayer captured forward -> pinned host out"},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks,
+        }
+        if base is not None:
+            line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind",
+                                                         "sample")}
+            line["parity_vs_oracle"] = base["parity"]
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is the route + permute
+    + layer of a bounded sample of the workload's tokens (as many tokens as
+    the host has cores, round robin over the batch), on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from grouped_expert_gemm_moe_gb300 import workloads as W
+    cfg, T, routing, _ = WORKLOADS[args.workload]
+    shape = W.CONFIGS[cfg]
+    inp = W.make_layer(shape, T, routing, seed=0, device="cpu")
+    wbits = (W.bf16_bits(inp.w_gu), W.bf16_bits(inp.w_down))
+    per = max(1, min(T, oracle.num_threads()))
+    def step(i):
+        tok = (np.arange(per) + i * per) % T
+        host = oracle_sample(inp, tok)
+        run_oracle_tokens(inp, host, tok, wbits)
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    sec = time.perf_counter() - t0
+    value = per * args.steps / sec
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": args.workload, "layer": shape.name, "T": T, "H": shape.H,
+                   "E": shape.E, "k": shape.k, "I": shape.I, "S": shape.S, "routing": routing},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": per, "kind": "oracle",
+                         "sample": f"per step: route+permute+layer of {per} of the {T} tokens"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

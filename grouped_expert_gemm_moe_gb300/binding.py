@@ -47,6 +47,10 @@ _SIGS = {
     "moe_grouped_gemm_swiglu_w8": ([P, P, I, I, I, I, P, P, P, P, P, P, SZ, P, P], I),
     "moe_grouped_gemv_w8": ([P, P, I, I, I, I, P, P, P, P, P, P, SZ, P, P], I),
     "moe_combine": ([P, P, P, I, I, I, I, P, P, P, P], I),
+    "moe_grouped_gemm_gate_up": ([P, P, I, I, I, I, P, P, P, P], I),
+    "moe_grouped_gemm_down": ([P, P, I, I, I, I, P, P, P, P], I),
+    "moe_grouped_gemv_gate_up": ([P, P, I, I, I, I, P, P, P, P], I),
+    "moe_grouped_gemv_down": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_quantize_w8": ([P, I64, I64, P, P], I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -182,6 +186,37 @@ def moe_grouped_gemv(x_perm, offsets, w_gu, w_down, y_perm, workspace, dev_error
     _ok(_lib.moe_grouped_gemv(_ptr(x_perm), _ptr(offsets), G, M, H, I_, _ptr(w_gu),
                               _ptr(w_down), _ptr(y_perm), _ptr(workspace), wsb, _ptr(dev_error),
                               _stream(stream)), "moe_grouped_gemv")
+
+
+def _phase(name, inp, offsets, w, out, H, I_, dev_error, stream):
+    _dev(inp, "input", torch.bfloat16); _dev(offsets, "offsets", torch.int32)
+    _dev(w, "weights", torch.bfloat16); _dev(out, "output", torch.bfloat16)
+    M = inp.shape[0]
+    G = offsets.numel() - 1
+    _ok(getattr(_lib, name)(_ptr(inp), _ptr(offsets), G, M, H, I_, _ptr(w), _ptr(out),
+                            _ptr(dev_error), _stream(stream)), name)
+
+
+def moe_grouped_gemm_gate_up(x_perm, offsets, w_gu, h, dev_error=None, stream=None):
+    """h [M,I] = silu(x_perm Wg^T) * (x_perm Wu^T) per group (tcgen05)."""
+    _phase("moe_grouped_gemm_gate_up", x_perm, offsets, w_gu, h, x_perm.shape[1], h.shape[1],
+           dev_error, stream)
+
+
+def moe_grouped_gemm_down(h, offsets, w_down, y_perm, dev_error=None, stream=None):
+    """y_perm [M,H] = h Wd^T per group (tcgen05)."""
+    _phase("moe_grouped_gemm_down", h, offsets, w_down, y_perm, y_perm.shape[1], h.shape[1],
+           dev_error, stream)
+
+
+def moe_grouped_gemv_gate_up(x_perm, offsets, w_gu, h, dev_error=None, stream=None):
+    _phase("moe_grouped_gemv_gate_up", x_perm, offsets, w_gu, h, x_perm.shape[1], h.shape[1],
+           dev_error, stream)
+
+
+def moe_grouped_gemv_down(h, offsets, w_down, y_perm, dev_error=None, stream=None):
+    _phase("moe_grouped_gemv_down", h, offsets, w_down, y_perm, y_perm.shape[1], h.shape[1],
+           dev_error, stream)
 
 
 def moe_grouped_gemm_swiglu_w8(x_perm, offsets, q_gu, s_gu, q_down, s_down, y_perm, workspace,

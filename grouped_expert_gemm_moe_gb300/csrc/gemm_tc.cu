@@ -351,10 +351,18 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
         return MOE_ERR_CUDA;
     const size_t smem = TcCfg<BN>::smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(tc_grouped_gemm<SWIGLU, BN>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    // raise the kernel's dynamic shared memory limit once per device (not on
+    // every call, so that launches can be captured into CUDA graphs)
+    static int attr_bytes[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (attr_bytes[dev] < static_cast<int>(smem)) {
+        const int want = max_smem_optin();
+        if (cudaFuncSetAttribute(tc_grouped_gemm<SWIGLU, BN>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, want) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_bytes[dev] = want;
+    }
     tc_grouped_gemm<SWIGLU, BN><<<sm_count(), TC_THREADS, smem, stream>>>(
         tm_act, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
@@ -367,6 +375,26 @@ moe_status check_ffn_args(const void *x_perm, const int32_t *offsets, int G, int
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" moe_status moe_grouped_gemm_gate_up(const uint16_t *x_perm, const int32_t *offsets,
+                                               int G, int M, int H, int I, const uint16_t *w_gu,
+                                               uint16_t *h, int32_t *dev_error,
+                                               cudaStream_t stream) {
+    moe_status st = check_ffn_args(x_perm, offsets, G, M, H, I, w_gu, w_gu, h, h,
+                                   moe_ffn_workspace_size(M, I), 8);
+    if (st != MOE_OK) return st;
+    return launch_tc<true, 256>(x_perm, w_gu, offsets, G, M, H, 2 * I, I, I, h, dev_error, stream);
+}
+
+extern "C" moe_status moe_grouped_gemm_down(const uint16_t *h, const int32_t *offsets, int G,
+                                            int M, int H, int I, const uint16_t *w_down,
+                                            uint16_t *y_perm, int32_t *dev_error,
+                                            cudaStream_t stream) {
+    moe_status st = check_ffn_args(h, offsets, G, M, H, I, w_down, w_down, y_perm, y_perm,
+                                   moe_ffn_workspace_size(M, I), 8);
+    if (st != MOE_OK) return st;
+    return launch_tc<false, 256>(h, w_down, offsets, G, M, I, H, H, 0, y_perm, dev_error, stream);
+}
 
 extern "C" moe_status moe_grouped_gemm_swiglu(const uint16_t *x_perm, const int32_t *offsets,
                                               int G, int M, int H, int I, const uint16_t *w_gu,

@@ -455,6 +455,40 @@ moe_status check_ffn_args(const void *x_perm, const int32_t *offsets, int G, int
 }
 }  // namespace moe
 
+namespace moe {
+static moe_status check_phase_args(const void *in, const int32_t *offsets, int G, int M, int H,
+                                   int I, const void *w, const void *out, int k_align) {
+    if (!in || !offsets || !w || !out || G < 1 || M < 1 || H < 1 || I < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (G > 1024) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(M) * H >= (1ll << 31) || static_cast<int64_t>(M) * I >= (1ll << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (H % k_align != 0 || I % k_align != 0) return MOE_ERR_ALIGNMENT;
+    if (!aligned16(in) || !aligned16(w) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+}  // namespace moe
+
+extern "C" moe_status moe_grouped_gemv_gate_up(const uint16_t *x_perm, const int32_t *offsets,
+                                               int G, int M, int H, int I, const uint16_t *w_gu,
+                                               uint16_t *h, int32_t *dev_error,
+                                               cudaStream_t stream) {
+    moe_status st = check_phase_args(x_perm, offsets, G, M, H, I, w_gu, h, 8);
+    if (st != MOE_OK) return st;
+    launch_gateup_bf16(pick_nch(H / 8), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
+    return launch_status();
+}
+
+extern "C" moe_status moe_grouped_gemv_down(const uint16_t *h, const int32_t *offsets, int G,
+                                            int M, int H, int I, const uint16_t *w_down,
+                                            uint16_t *y_perm, int32_t *dev_error,
+                                            cudaStream_t stream) {
+    moe_status st = check_phase_args(h, offsets, G, M, H, I, w_down, y_perm, 8);
+    if (st != MOE_OK) return st;
+    launch_down_bf16(pick_nch(I / 8), stream, h, offsets, G, M, H, I, w_down, y_perm, dev_error);
+    return launch_status();
+}
+
 extern "C" moe_status moe_grouped_gemv(const uint16_t *x_perm, const int32_t *offsets, int G,
                                        int M, int H, int I, const uint16_t *w_gu,
                                        const uint16_t *w_down, uint16_t *y_perm, void *workspace,

@@ -166,10 +166,19 @@ extern "C" moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, 
     int nt = 32;
     while (nt < nt_max && static_cast<int64_t>(nt) * 8 < n) nt *= 2;
     const size_t smem = static_cast<size_t>(E) * nt * 4;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(permute_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PERM_SMEM_BUDGET) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (smem > 48 * 1024) {
+        // once per device, so that launches can be captured into CUDA graphs
+        static bool attr_set[64] = {false};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(permute_index_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     PERM_SMEM_BUDGET) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            attr_set[dev] = true;
+        }
+    }
     permute_index_kernel<<<1, nt, smem, stream>>>(topk_ids, T, E, S, k, offsets, sorted_slot,
                                                    row_of_slot, dev_error);
     moe_status st = launch_status();

@@ -92,6 +92,21 @@ class MoELayer:
         B.moe_permute(b.topk_ids, self.E, self.S, x, b.offsets, b.sorted_slot, b.row_of_slot,
                       b.x_perm, None, self.err, stream)
 
+    def hidden(self, b: LayerBuffers) -> torch.Tensor:
+        """The bf16 hidden rows h [M, I] inside the FFN workspace."""
+        M = self.rows(b.T)
+        return b.ffn_ws[:M * self.I * 2].view(torch.bfloat16).view(M, self.I)
+
+    def gate_up(self, b: LayerBuffers, kind: str, stream=None):
+        """First FFN phase alone (bf16 experts): h = silu(x Wg^T) * (x Wu^T)."""
+        fn = B.moe_grouped_gemv_gate_up if kind == "gemv" else B.moe_grouped_gemm_gate_up
+        fn(b.x_perm, b.offsets, self.w_gu, self.hidden(b), self.err, stream)
+
+    def down(self, b: LayerBuffers, kind: str, stream=None):
+        """Second FFN phase alone (bf16 experts): y_perm = h Wd^T."""
+        fn = B.moe_grouped_gemv_down if kind == "gemv" else B.moe_grouped_gemm_down
+        fn(self.hidden(b), b.offsets, self.w_down, b.y_perm, self.err, stream)
+
     def ffn(self, b: LayerBuffers, kind: str, stream=None):
         if self.int8:
             fn = B.moe_grouped_gemv_w8 if kind == "gemv" else B.moe_grouped_gemm_swiglu_w8
@@ -116,9 +131,37 @@ class MoELayer:
         self.combine(b, dst, residual, stream)
         return dst
 
+    def capture(self, x: torch.Tensor, logits: torch.Tensor, out=None, residual=None,
+                ffn="auto") -> "CapturedForward":
+        """Record one forward pass over the fixed device buffers x / logits
+        into a CUDA graph; replay() then reruns it with whatever x and
+        logits hold.  Decode-sized batches are launch-bound without this."""
+        return CapturedForward(self, x, logits, out, residual, ffn)
+
     def check(self):
         """Synchronise and raise if any kernel reported a device-side fault."""
         B.check_device_error(self.err, "MoELayer")
+
+
+class CapturedForward:
+    """A forward pass recorded into a CUDA graph (see MoELayer.capture)."""
+
+    def __init__(self, layer: MoELayer, x, logits, out, residual, ffn):
+        self.layer, self.x, self.logits = layer, x, logits
+        T = x.shape[0]
+        self.out = out if out is not None else torch.empty((T, layer.H), dtype=torch.bfloat16,
+                                                           device=x.device)
+        # one eager pass first: sets kernel attributes outside the capture
+        layer.forward(x, logits, out=self.out, residual=residual, ffn=ffn)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            layer.forward(x, logits, out=self.out, residual=residual, ffn=ffn)
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
 
 
 class MoEStack:

@@ -160,11 +160,33 @@ moe_status moe_grouped_gemv(const uint16_t *x_perm, const int32_t *offsets, int 
                             int32_t *dev_error, cudaStream_t stream);
 
 /*
+ * The two phases of each grouped FFN as separate calls (the combined calls
+ * above are exactly gate_up followed by down), for callers that schedule
+ * or time them separately:
+ *   *_gate_up: h [M,I] bf16 = silu(x_perm . Wg^T) * (x_perm . Wu^T), per group;
+ *   *_down   : y_perm [M,H] bf16 = h . Wd^T, per group.
+ * h is caller-owned device memory (16-byte aligned, M*I bf16).
+ */
+moe_status moe_grouped_gemm_gate_up(const uint16_t *x_perm, const int32_t *offsets, int G, int M,
+                                    int H, int I, const uint16_t *w_gu, uint16_t *h,
+                                    int32_t *dev_error, cudaStream_t stream);
+moe_status moe_grouped_gemm_down(const uint16_t *h, const int32_t *offsets, int G, int M, int H,
+                                 int I, const uint16_t *w_down, uint16_t *y_perm,
+                                 int32_t *dev_error, cudaStream_t stream);
+moe_status moe_grouped_gemv_gate_up(const uint16_t *x_perm, const int32_t *offsets, int G, int M,
+                                    int H, int I, const uint16_t *w_gu, uint16_t *h,
+                                    int32_t *dev_error, cudaStream_t stream);
+moe_status moe_grouped_gemv_down(const uint16_t *h, const int32_t *offsets, int G, int M, int H,
+                                 int I, const uint16_t *w_down, uint16_t *y_perm,
+                                 int32_t *dev_error, cudaStream_t stream);
+
+/*
  * int8 weight-only variants ("dispatch" README, phase 5a: per-channel int8
  * weight-only quantisation).  q_gu: [G,2I,H] int8 with s_gu: [G,2I] fp32
  * (one scale per output row); q_down: [G,H,I] int8 with s_down: [G,H].
  * The effective weight is (float)q * scale; the kernels accumulate
- * sum x*q in fp32 and multiply by the row's scale.  Otherwise as above.
+ * sum x*q in fp32 and multiply by the row's scale.  H and I must be
+ * multiples of 16.  Otherwise as above.
  */
 moe_status moe_grouped_gemm_swiglu_w8(const uint16_t *x_perm, const int32_t *offsets, int G,
                                       int M, int H, int I, const int8_t *q_gu, const float *s_gu,
