@@ -52,6 +52,7 @@ _SIGS = {
     "moe_grouped_gemv_gate_up": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_grouped_gemv_down": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_quantize_w8": ([P, I64, I64, P, P], I),
+    "moe_grouped_gemv_noalloc": ([P, P, I, I, I, I, P, P, P, P, P], I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -217,6 +218,22 @@ def moe_grouped_gemv_gate_up(x_perm, offsets, w_gu, h, dev_error=None, stream=No
 def moe_grouped_gemv_down(h, offsets, w_down, y_perm, dev_error=None, stream=None):
     _phase("moe_grouped_gemv_down", h, offsets, w_down, y_perm, y_perm.shape[1], h.shape[1],
            dev_error, stream)
+
+
+def moe_grouped_gemv_noalloc(x_perm, offsets, w_gu, w_down, y_perm, dev_error=None,
+                             stream=None):
+    """moe_grouped_gemv with its scratch in the library's built-in 8 MiB
+    array instead of a caller workspace (M * I <= 4,194,304).  Calls that
+    may overlap on the GPU share that array and must be serialised."""
+    _dev(x_perm, "x_perm", torch.bfloat16); _dev(offsets, "offsets", torch.int32)
+    _dev(y_perm, "y_perm", torch.bfloat16)
+    _dev(w_gu, "w_gu", torch.bfloat16); _dev(w_down, "w_down", torch.bfloat16)
+    M, H = x_perm.shape
+    G = offsets.numel() - 1
+    I_ = w_down.shape[2]
+    _ok(_lib.moe_grouped_gemv_noalloc(_ptr(x_perm), _ptr(offsets), G, M, H, I_, _ptr(w_gu),
+                                      _ptr(w_down), _ptr(y_perm), _ptr(dev_error),
+                                      _stream(stream)), "moe_grouped_gemv_noalloc")
 
 
 def moe_grouped_gemm_swiglu_w8(x_perm, offsets, q_gu, s_gu, q_down, s_down, y_perm, workspace,

@@ -17,6 +17,7 @@
 // warp keeps 8 KB in flight.  A group with more rows than NR is processed
 // in blocks of NR rows (the weight row is re-read from L2).
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -521,5 +522,69 @@ extern "C" moe_status moe_grouped_gemv_w8(const uint16_t *x_perm, const int32_t 
     if ((st = launch_status()) != MOE_OK) return st;
     launch_down_w8(pick_nch(I / 16), stream, static_cast<const uint16_t *>(h), offsets, G, M, H, I,
                    q_down, s_down, y_perm, dev_error);
+    return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// moe_grouped_gemv_noalloc: the grouped GEMV for callers that cannot allocate
+// device memory.  Its only scratch, the bf16 hidden rows h [M, I], lives in
+// the file-scope array below instead of a caller workspace.  The array is
+// part of this library's device image, so every GPU that loads the library
+// holds these bytes until the process exits.
+
+namespace moe {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(8) << 20;   // 8 MiB: M * I <= 4,194,304
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name only stands for the symbol; the address a kernel can use
+// is looked up once per device (with that device current) and cached.
+static uint16_t *noalloc_scratch(moe_status *st) {
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *st = MOE_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            *st = MOE_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return static_cast<uint16_t *>(addr[dev]);
+}
+
+}  // namespace moe
+
+extern "C" moe_status moe_grouped_gemv_noalloc(const uint16_t *x_perm, const int32_t *offsets,
+                                               int G, int M, int H, int I, const uint16_t *w_gu,
+                                               const uint16_t *w_down, uint16_t *y_perm,
+                                               int32_t *dev_error, cudaStream_t stream) {
+    if (!x_perm || !offsets || !w_gu || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (G < 1 || M < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+    if (G > 1024) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(M) * H >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+    if (H % 8 != 0 || I % 8 != 0) return MOE_ERR_ALIGNMENT;
+    if (!aligned16(x_perm) || !aligned16(w_gu) || !aligned16(w_down) || !aligned16(y_perm))
+        return MOE_ERR_ALIGNMENT;
+    // the built-in scratch holds h = M x I bf16; a larger problem is refused
+    if (static_cast<size_t>(M) * static_cast<size_t>(I) * 2 > NOALLOC_SCRATCH_BYTES)
+        return MOE_ERR_WORKSPACE;
+    moe_status st = MOE_OK;
+    uint16_t *h = noalloc_scratch(&st);
+    if (h == nullptr) return st;
+    // Nothing in the scratch has to start at zero: the gate/up pass writes
+    // every h row of every non-empty group before the down pass reads it.
+    launch_gateup_bf16(pick_nch(H / 8), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
+    if ((st = launch_status()) != MOE_OK) return st;
+    launch_down_bf16(pick_nch(I / 8), stream, static_cast<const uint16_t *>(h), offsets, G, M, H,
+                     I, w_down, y_perm, dev_error);
     return launch_status();
 }

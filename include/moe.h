@@ -200,6 +200,30 @@ moe_status moe_grouped_gemv_w8(const uint16_t *x_perm, const int32_t *offsets, i
                                cudaStream_t stream);
 
 /*
+ * moe_grouped_gemv_noalloc -- moe_grouped_gemv without a workspace argument,
+ * for callers that cannot allocate device memory: code running inside a host
+ * framework's execute callback that hands out no allocator, latency-critical
+ * paths that cannot afford the device-wide synchronisation cudaMalloc and
+ * cudaFree may cause, and processes whose device memory is already handed to
+ * a pool of their own.  The pages have no counterpart of this call.
+ * The hidden rows h [M,I] go to an 8 MiB scratch array built into the
+ * library (every GPU that loads libmoe.so holds it until the process exits),
+ * so M * I must be at most 4,194,304; a larger problem returns
+ * MOE_ERR_WORKSPACE without launching anything.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array and leaves its
+ * contents behind: calls whose kernels may overlap on the GPU (different
+ * streams without ordering between them) race on it and must be serialised
+ * by the caller.  No part of the array needs to start at zero.  Arguments
+ * and results are otherwise those of moe_grouped_gemv; no allocation of any
+ * kind is made.
+ */
+moe_status moe_grouped_gemv_noalloc(const uint16_t *x_perm, const int32_t *offsets, int G, int M,
+                                    int H, int I, const uint16_t *w_gu, const uint16_t *w_down,
+                                    uint16_t *y_perm, int32_t *dev_error, cudaStream_t stream);
+
+/*
  * moe_combine -- weighted sum of each token's expert rows back in token
  * order, by gathering (no scatter-add, so the result is the same bytes on
  * every run; the "Phase 6" pull request of "dispatch", Summary, reports
