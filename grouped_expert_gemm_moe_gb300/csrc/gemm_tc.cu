@@ -26,16 +26,9 @@
 // MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <algorithm>
 
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
-
-constexpr int TC_BM = 128;        // token rows per tile (MMA M)
-constexpr int TC_BK = 64;         // K per stage: one 128-byte swizzle row of bf16
-constexpr int TC_THREADS = 192;   // 6 warps
-constexpr int TC_ABOX = 16;       // rows per activation TMA box
 
 template <int BN>
 struct TcCfg {
@@ -50,32 +43,6 @@ struct TcCfg {
                2 * static_cast<size_t>(G + 1) * sizeof(int);
     }
 };
-
-struct TileInfo {
-    int g, nt, m0, nrows;
-};
-
-// s_tile[g] = first linear tile of group g (s_tile[G] = total).
-__device__ __forceinline__ TileInfo decode_tile(int t, const int *s_tile, const int *s_off, int G) {
-    int lo = 0, hi = G - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_tile[mid] <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    TileInfo ti;
-    ti.g = lo;
-    const int u = t - s_tile[lo];
-    const int rows = s_off[lo + 1] - s_off[lo];
-    const int mt_count = (rows + TC_BM - 1) / TC_BM;
-    ti.nt = u / mt_count;
-    const int mt = u - ti.nt * mt_count;
-    ti.m0 = s_off[lo] + mt * TC_BM;
-    ti.nrows = min(TC_BM, rows - mt * TC_BM);
-    return ti;
-}
-
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // SWIGLU: out = h [M, NOUT=I], weights [G*2I, K=H], up rows at +UP_OFF = I.
 // PLAIN : out = y [M, NOUT=H], weights [G*H,  K=I].
@@ -123,31 +90,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         prefetch_tmap(&tm_w);
     }
     if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
-    if (warp == 2) {
-        // tile table: tiles of group g = n_tiles * ceil(rows_g / 128)
-        int carry = 0;
-        bool bad = false;
-        for (int base = 0; base < G; base += 32) {
-            const int g = base + lane;
-            int tiles = 0;
-            if (g < G) {
-                const int o0 = offsets[g], o1 = offsets[g + 1];
-                if (o0 < 0 || o1 < o0 || o1 > M) bad = true;
-                else tiles = ((o1 - o0 + TC_BM - 1) / TC_BM) * n_tiles;
-                s_off[g] = o0;
-                if (g == G - 1) s_off[G] = o1;
-            }
-            const int inc = warp_inclusive_scan(tiles);
-            if (g < G) s_tile[g] = carry + inc - tiles;
-            carry += __shfl_sync(FULL, inc, 31);
-        }
-        bad = __any_sync(FULL, bad);
-        if (lane == 0) {
-            s_tile[G] = carry;
-            *s_total = bad ? 0 : carry;
-            if (bad) report(dev_error, MOE_ERR_DEVICE_CHECK);
-        }
-    }
+    if (warp == 2) build_tile_table(offsets, G, M, n_tiles, s_off, s_tile, s_total, dev_error);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -314,33 +257,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 // ------------------------------------------------------------------ host
 
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 2-D bf16 tensor [outer, inner] row-major, box [box_outer, 64], 128-byte swizzle.
-static bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
-                           uint32_t box_outer) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(TC_BK), box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool SWIGLU, int BN>
 static moe_status launch_tc(const void *act, const void *w, const int32_t *offsets, int G, int M,
                             int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
@@ -351,26 +267,12 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
         return MOE_ERR_CUDA;
     const size_t smem = TcCfg<BN>::smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
-    // raise the kernel's dynamic shared memory limit once per device (not on
-    // every call, so that launches can be captured into CUDA graphs)
-    static int attr_bytes[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (attr_bytes[dev] < static_cast<int>(smem)) {
-        const int want = max_smem_optin();
-        if (cudaFuncSetAttribute(tc_grouped_gemm<SWIGLU, BN>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, want) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_bytes[dev] = want;
-    }
+    static int attr_done[64] = {0};
+    if (!raise_smem_limit(tc_grouped_gemm<SWIGLU, BN>, attr_done)) return MOE_ERR_CUDA;
     tc_grouped_gemm<SWIGLU, BN><<<sm_count(), TC_THREADS, smem, stream>>>(
         tm_act, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
 }
-
-moe_status check_ffn_args(const void *x_perm, const int32_t *offsets, int G, int M, int H, int I,
-                          const void *w_gu, const void *w_down, const void *y_perm,
-                          const void *workspace, size_t workspace_bytes, int k_align);
 
 }  // namespace moe
 
@@ -408,16 +310,4 @@ extern "C" moe_status moe_grouped_gemm_swiglu(const uint16_t *x_perm, const int3
     st = launch_tc<true, 256>(x_perm, w_gu, offsets, G, M, H, 2 * I, I, I, h, dev_error, stream);
     if (st != MOE_OK) return st;
     return launch_tc<false, 256>(h, w_down, offsets, G, M, I, H, H, 0, y_perm, dev_error, stream);
-}
-
-extern "C" moe_status moe_grouped_gemm_swiglu_w8(const uint16_t *x_perm, const int32_t *offsets,
-                                                 int G, int M, int H, int I, const int8_t *q_gu,
-                                                 const float *s_gu, const int8_t *q_down,
-                                                 const float *s_down, uint16_t *y_perm,
-                                                 void *workspace, size_t workspace_bytes,
-                                                 int32_t *dev_error, cudaStream_t stream) {
-    (void)x_perm; (void)offsets; (void)G; (void)M; (void)H; (void)I; (void)q_gu; (void)s_gu;
-    (void)q_down; (void)s_down; (void)y_perm; (void)workspace; (void)workspace_bytes;
-    (void)dev_error; (void)stream;
-    return MOE_ERR_UNSUPPORTED;
 }

@@ -1,0 +1,162 @@
+"""int8 weight-only experts and the 16-layer stack against the oracle.
+
+int8: the "dispatch" README's phase 5a scheme (per-output-channel int8
+weights, fp32 scales, bf16 activations).  The library's host quantiser must
+match the oracle's bit for bit; the tensor-core GEMM and the GEMV must match
+the oracle's layer on the same q and scales (which dequantises as
+(float)q * scale) within the bf16 bounds.
+
+Stack: 16 OLMoE-shaped MoE blocks with residual adds, skewed so the busiest
+expert gets about 4x the mean load (the "switchyard" page, 03 Load balance).
+Checked layer by layer with the oracle fed the GPU's own x_l and router
+logits (teacher forcing), so a routing near-tie cannot compound across layers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from grouped_expert_gemm_moe_gb300 import workloads as W
+
+from gpu_helpers import W_RTOL, assert_close, errors, sample_tokens, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def mods():
+    import __graft_entry__ as g
+    g.build()
+    from grouped_expert_gemm_moe_gb300 import binding, layer
+    return binding, layer
+
+
+_W8 = {}
+
+
+def w8_layer(B, L, seed=0):
+    if "layer" not in _W8:
+        sh = W.OLMOE_W8
+        inp = W.make_layer(sh, 1, "uniform", seed=seed, device=DEV)
+        q_gu, s_gu = B.moe_quantize_w8(inp.w_gu)
+        q_down, s_down = B.moe_quantize_w8(inp.w_down)
+        layer = L.MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize, q_gu=q_gu.to(DEV),
+                           s_gu=s_gu.to(DEV), q_down=q_down.to(DEV), s_down=s_down.to(DEV),
+                           device=DEV)
+        _W8.update(layer=layer, inp=inp, host=(q_gu.numpy(), s_gu.numpy(), q_down.numpy(),
+                                                 s_down.numpy()))
+    return _W8["layer"], _W8["inp"], _W8["host"]
+
+
+def batch(sh, T, routing, w_r, seed):
+    g = W.make_generator(seed + 101 * T)
+    x = torch.randn((T, sh.H), generator=g).to(torch.bfloat16)
+    bias = W.routing_bias(sh, routing)
+    return x, W.router_logits_input(x, w_r.cpu(), bias)
+
+
+@pytest.mark.parametrize("ffn", ["gemm", "gemv"])
+@pytest.mark.parametrize("T,routing", [(1, "uniform"), (8, "zipf"), (16, "uniform"),
+                                       (64, "zipf"), (128, "uniform"), (512, "zipf"),
+                                       (2048, "uniform"), (2048, "zipf")])
+def test_w8_layer_matches_oracle(mods, T, routing, ffn):
+    B, L = mods
+    if ffn == "gemv" and T > 128:
+        pytest.skip("the GEMV is for decode-sized batches")
+    layer, inp, (qg, sg, qd, sd) = w8_layer(B, L)
+    sh = W.OLMOE_W8
+    x, logits = batch(sh, T, routing, inp.w_r, 3)
+    out = layer.forward(x.to(DEV), logits.to(DEV), ffn=ffn)
+    layer.check()
+    tok = sample_tokens(T)
+    ids, w = oracle.route(logits.numpy(), sh.k, sh.renormalize)
+    np.testing.assert_array_equal(layer.buffers(T).topk_ids.cpu().numpy(), ids)
+    y = oracle.moe_layer_w8(W.bf16_bits(x), ids, w, sh.E, sh.S, qg, sg, qd, sd, tokens=tok)
+    rel, mx = assert_close(to_np(out)[tok], y, f"w8 {ffn} T={T} {routing}")
+    print(f"w8 {ffn} T={T} {routing}: rel {rel:.2e} max {mx:.2e}")
+
+
+@pytest.mark.parametrize("H,I,E,S,k,T", [(144, 208, 5, 1, 2, 300), (256, 512, 4, 0, 1, 1000)])
+def test_w8_gemm_rows_vs_oracle(mods, H, I, E, S, k, T):
+    """Every permuted row of the int8 tensor-core FFN on ragged tiles."""
+    B, L = mods
+    sh = W.MoEShape("t8", H=H, E=E, k=k, I=I, S=S)
+    inp = W.make_layer(sh, T, "uniform", seed=5)
+    q_gu, s_gu = B.moe_quantize_w8(inp.w_gu)
+    q_down, s_down = B.moe_quantize_w8(inp.w_down)
+    layer = L.MoELayer(H, E, k, I, S, False, q_gu=q_gu.to(DEV), s_gu=s_gu.to(DEV),
+                       q_down=q_down.to(DEV), s_down=s_down.to(DEV), device=DEV)
+    b = layer.buffers(T)
+    layer.route(inp.logits.to(DEV), b)
+    layer.permute(inp.x.to(DEV), b)
+    layer.ffn(b, "gemm")
+    layer.check()
+    off = b.offsets.cpu().numpy()
+    xv = (W.bf16_bits(b.x_perm).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    M = layer.rows(T)
+    ref = np.zeros((M, H))
+    qg, sg, qd, sd = q_gu.numpy(), s_gu.numpy(), q_down.numpy(), s_down.numpy()
+    for g in range(E + S):
+        wg = (qg[g].astype(np.float32) * sg[g][:, None]).astype(np.float64)
+        wd = (qd[g].astype(np.float32) * sd[g][:, None]).astype(np.float64)
+        r0, r1 = off[g], off[g + 1]
+        z = xv[r0:r1]
+        hh = (z @ wg[:I].T) / (1 + np.exp(-(z @ wg[:I].T))) * (z @ wg[I:].T)
+        ref[r0:r1] = hh @ wd.T
+    rel, mx = errors(to_np(b.y_perm)[:M], ref)
+    assert rel <= 5e-3 and mx <= 2e-2, f"rel {rel:.3e} max {mx:.3e}"
+
+
+def test_w8_gemm_deterministic_and_agrees_with_gemv(mods):
+    B, L = mods
+    layer, inp, _ = w8_layer(B, L)
+    sh = W.OLMOE_W8
+    x, logits = batch(sh, 64, "uniform", inp.w_r, 9)
+    xd, ld = x.to(DEV), logits.to(DEV)
+    g1 = layer.forward(xd, ld, ffn="gemm").clone()
+    g2 = layer.forward(xd, ld, ffn="gemm").clone()
+    v = layer.forward(xd, ld, ffn="gemv").clone()
+    layer.check()
+    assert torch.equal(g1, g2)
+    rel, mx = errors(to_np(g1), to_np(v))
+    assert rel < 5e-3 and mx < 2e-2
+
+
+@pytest.mark.parametrize("T,ffn", [(64, "gemm"), (2048, "gemm")])
+def test_stack_teacher_forced(mods, T, ffn):
+    B, L = mods
+    sh = W.OLMOE_STACK
+    x0, layers_w, bias = W.make_stack(sh, T, "skew4", seed=0, device=DEV)
+    layers = [L.MoELayer(sh.H, sh.E, sh.k, sh.I, 0, False, w_gu=wg, w_down=wd, device=DEV)
+              for (_, wg, wd) in layers_w]
+    routers = [wr for (wr, _, _) in layers_w]
+    stack = L.MoEStack(layers, routers, bias)
+    keep = []
+    final = stack.forward(x0, ffn=ffn, keep=keep).clone()
+    for layer in layers:
+        layer.check()
+    tok = sample_tokens(T, n=16)
+    bias_np = bias.cpu().numpy()
+    worst = 0.0
+    max_load = []
+    for l, ((x_l, logits_l), layer) in enumerate(zip(keep, layers)):
+        x_next = keep[l + 1][0] if l + 1 < len(keep) else final
+        xb = W.bf16_bits(x_l)
+        lg = logits_l.cpu().numpy()
+        # router logits kernel vs the oracle (fp64) on the sampled tokens
+        ref_logits = oracle.router_logits(xb[tok], W.bf16_bits(routers[l]), bias_np)
+        assert np.abs(lg[tok] - ref_logits).max() <= 1e-4 * np.abs(ref_logits).max()
+        ids, w = oracle.route(lg, sh.k, sh.renormalize)
+        np.testing.assert_array_equal(layer.buffers(T).topk_ids.cpu().numpy(), ids)
+        cnt = np.bincount(ids.ravel(), minlength=sh.E)
+        max_load.append(cnt.max() / (T * sh.k / sh.E))
+        y = oracle.moe_layer(xb, ids, w, sh.E, 0, W.bf16_bits(layers_w[l][1]),
+                             W.bf16_bits(layers_w[l][2]), residual_bits=xb, tokens=tok)
+        rel, mx = assert_close(to_np(x_next)[tok], y, f"stack layer {l}")
+        worst = max(worst, rel)
+    print(f"stack T={T}: worst per-layer rel {worst:.2e}; max/mean load per layer "
+          f"{np.round(max_load, 2).tolist()}")
+    if T == 2048:
+        assert 3.5 <= max_load[0] <= 4.5
