@@ -209,8 +209,7 @@ class Phases:
         b = self.b = layer.buffers(x.shape[0])
 
         def pre():
-            layer.route(logits, b)
-            layer.permute(x, b)
+            layer.route_permute(logits, x, b)
 
         def mid():
             layer.gate_up(b, kind)
@@ -245,13 +244,40 @@ class Phases:
         e.record()
 
 
-KERNELS_PER_STEP = 6      # route, permute index, permute gather, gate/up, down, combine
+def kernels_per_step(layer, T):
+    """Kernels of one layer step: route + permute (1 fused launch for small
+    batches; else the routing kernel plus 1 permute kernel up to 1024 slots
+    or 3 above), then gate/up, down and combine."""
+    if layer.fused_route_permute_ok(T):
+        rp = 1
+    else:
+        rp = 1 + (1 if T * layer.k <= 1024 else 3)
+    return rp + 3
 
 
 def touched_groups(layer, b):
     import numpy as np
     off = b.offsets.cpu().numpy()
     return int(np.count_nonzero(np.diff(off) > 0))
+
+
+def time_graph(cap, K, W, flush):
+    """W warm-up steps, then K timed steps of a captured forward pass, L2
+    flushed before each step; per-step device times (ms)."""
+    import torch
+    for _ in range(W):
+        flush.zero_()
+        cap.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for a, b in evs:
+        flush.zero_()
+        a.record()
+        cap.replay()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
 
 
 def time_steps(phases, K, W, flush):
@@ -313,9 +339,14 @@ def kernel_roofline(shape, T, n_groups, gate_up_ms, peaks, kind, workload):
 
 
 def measure_T(layer, shape, T, x, logits, K, W, flush, peaks, workload):
+    """Layer time from K steps of the whole forward pass captured in one
+    CUDA graph; the gate/up kernel's time from K further steps recorded as
+    three graphs with events around the gate/up launch."""
     kind = layer.choose_ffn(T)
+    cap = layer.capture(x, logits, ffn=kind)
+    step = time_graph(cap, K, W, flush)
     ph = Phases(layer, x, logits, kind)
-    step, gu = time_steps(ph, K, W, flush)
+    _, gu = time_steps(ph, K, W, flush)
     n_groups = touched_groups(layer, ph.b)
     ms = statistics.fmean(step)
     roof = layer_roofline(shape, T, n_groups, peaks)
@@ -485,8 +516,10 @@ def run_ours(args):
                        "routing": routing, "ffn": m["kind"], "served_groups": m["n_groups"],
                        "l2": "flushed between steps (256 MiB write, outside the timed events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "timing": "CUDA events per step on the launch stream; step = 3 graph "
-                                 "launches [route+permute][gate/up][down+combine]"},
+                       "timing": "CUDA events around each step on the launch stream; a step "
+                                 "is one CUDA graph of the whole layer; the gate/up kernel is "
+                                 "timed over K more steps recorded as three graphs "
+                                 "[route+permute][gate/up][down+combine]"},
             "us_per_layer": round(m["ms"] * 1e3, 2),
             "layer_roofline": {"t_roof_us": round(roof["t_roof_us"], 2), "bound": roof["bound"],
                                "frac": round(roof["t_roof_us"] / (m["ms"] * 1e3), 4),
@@ -498,7 +531,7 @@ def run_ours(args):
                     "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": round(e2e_ms * 1e3, 2),
                     "path": "pinned host x+logits -> MoELayer captured forward -> pinned host out"},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": 2 * kernels_per_step(layer, T) * args.steps,   # both timed passes
             "clocks": clocks,
         }
         if base is not None:

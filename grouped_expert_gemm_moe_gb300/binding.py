@@ -53,6 +53,7 @@ _SIGS = {
     "moe_grouped_gemv_down": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_quantize_w8": ([P, I64, I64, P, P], I),
     "moe_grouped_gemv_noalloc": ([P, P, I, I, I, I, P, P, P, P, P], I),
+    "moe_route_permute": ([P, I, I, I, I, I, P, I, I, P, P, P, P, P, P, P, P], I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -155,6 +156,33 @@ def moe_permute(topk_ids, E, S, x, offsets, sorted_slot, row_of_slot, x_perm, wo
     _ok(_lib.moe_permute(_ptr(topk_ids), T, E, S, k, _ptr(x), xd, H, _ptr(offsets),
                          _ptr(sorted_slot), _ptr(row_of_slot), _ptr(x_perm), _ptr(workspace),
                          wsb, _ptr(dev_error), _stream(stream)), "moe_permute")
+
+
+ROUTE_PERMUTE_MAX_SLOTS = 1024
+ROUTE_PERMUTE_MAX_E = 256
+
+
+def moe_route_permute(logits, k, renormalize, S, x, topk_ids, topk_w, offsets, sorted_slot,
+                      row_of_slot, x_perm, dev_error=None, stream=None):
+    """moe_route + moe_permute in one launch (T*k <= 1024, E <= 256)."""
+    _dev(logits, "logits", torch.float32)
+    T, E = logits.shape
+    _dev(x, "x")
+    if x.dtype == torch.bfloat16:
+        xd = MOE_DTYPE_BF16
+    elif x.dtype == torch.float32:
+        xd = MOE_DTYPE_F32
+    else:
+        raise ValueError("x must be bf16 or fp32")
+    _dev(topk_ids, "topk_ids", torch.int32); _dev(topk_w, "topk_w", torch.float32)
+    for n, t in (("offsets", offsets), ("sorted_slot", sorted_slot),
+                 ("row_of_slot", row_of_slot)):
+        _dev(t, n, torch.int32)
+    _dev(x_perm, "x_perm", torch.bfloat16)
+    _ok(_lib.moe_route_permute(_ptr(logits), T, E, S, k, int(bool(renormalize)), _ptr(x), xd,
+                               x.shape[1], _ptr(topk_ids), _ptr(topk_w), _ptr(offsets),
+                               _ptr(sorted_slot), _ptr(row_of_slot), _ptr(x_perm),
+                               _ptr(dev_error), _stream(stream)), "moe_route_permute")
 
 
 def moe_ffn_workspace_size(M, I) -> int:

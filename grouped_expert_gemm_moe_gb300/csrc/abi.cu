@@ -1,6 +1,7 @@
 // abi.cu -- host-side pieces of the C ABI: status strings, device queries,
 // and the offline int8 quantiser.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -40,6 +41,14 @@ int max_smem_optin() {
     if (cudaGetDevice(&dev) != cudaSuccess) return 48 * 1024;
     query_device(dev);
     return (dev >= 0 && dev < 64) ? g_smem_optin[dev] : 48 * 1024;
+}
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("MOE_DISABLE_PDL");
+        return !(v && v[0] == '1');
+    }();
+    return on;
 }
 
 }  // namespace moe

@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(256) combine_kernel(
     const uint16_t *__restrict__ y_perm, const int32_t *__restrict__ row_of_slot,
     const float *__restrict__ topk_w, int T, int k, int S, int H,
     const uint16_t *residual, uint16_t *out, int32_t *dev_error) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;     // 8-element chunk
     if (c * 8 >= H) return;
@@ -22,8 +24,11 @@ __global__ void __launch_bounds__(256) combine_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 
-    auto add_row = [&](int64_t r, float w) {
-        const uint4 v = ld_nc(y_perm + r * H + c * 8);
+    // issue the loads of up to 8 routed rows at once (their indices and
+    // weights first, then the rows), so the gathers overlap instead of
+    // paying one memory latency per expert in turn; sums stay in j order
+    constexpr int BATCH = 8;
+    auto accumulate = [&](const uint4 &v, float w) {
         const uint32_t p[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -31,16 +36,38 @@ __global__ void __launch_bounds__(256) combine_kernel(
             acc[2 * i + 1] = fmaf(w, bf_hi(p[i]), acc[2 * i + 1]);
         }
     };
-    for (int j = 0; j < k; ++j) {
-        const int64_t slot = static_cast<int64_t>(t) * k + j;
-        const int64_t r = row_of_slot[slot];
-        if (r < 0 || r >= n) {
-            report(dev_error, MOE_ERR_DEVICE_CHECK);
-            continue;
+    for (int j0 = 0; j0 < k; j0 += BATCH) {              // routed rows, j ascending
+        int64_t r[BATCH];
+        float w[BATCH];
+        bool ok[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            ok[j] = false;
+            if (j0 + j < k) {
+                const int64_t slot = static_cast<int64_t>(t) * k + j0 + j;
+                r[j] = row_of_slot[slot];
+                w[j] = topk_w[slot];
+                ok[j] = r[j] >= 0 && r[j] < n;
+                if (!ok[j]) report(dev_error, MOE_ERR_DEVICE_CHECK);
+            }
         }
-        add_row(r, topk_w[slot]);
+        uint4 v[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j)
+            if (ok[j]) v[j] = ld_nc(y_perm + r[j] * H + c * 8);
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j)
+            if (ok[j]) accumulate(v[j], w[j]);
     }
-    for (int s = 0; s < S; ++s) add_row(n + static_cast<int64_t>(s) * T + t, 1.0f);
+    for (int s0 = 0; s0 < S; s0 += BATCH) {              // shared rows, s ascending
+        uint4 v[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j)
+            if (s0 + j < S) v[j] = ld_nc(y_perm + (n + static_cast<int64_t>(s0 + j) * T + t) * H + c * 8);
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j)
+            if (s0 + j < S) accumulate(v[j], 1.0f);
+    }
     if (residual) {
         const uint4 v = ld_nc(residual + static_cast<int64_t>(t) * H + c * 8);
         const uint32_t p[4] = {v.x, v.y, v.z, v.w};
@@ -76,7 +103,7 @@ extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_
     const int chunks = H / 8;
     const int threads = chunks >= 256 ? 256 : ((chunks + 31) / 32) * 32;
     dim3 grid((chunks + threads - 1) / threads, T);
-    combine_kernel<<<grid, threads, 0, stream>>>(y_perm, row_of_slot, topk_w, T, k, S, H, residual,
+    launch(combine_kernel, grid, threads, 0, stream, y_perm, row_of_slot, topk_w, T, k, S, H, residual,
                                                  out, dev_error);
     return launch_status();
 }

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
@@ -29,7 +31,39 @@ inline moe_status launch_status() {
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Launch with programmatic dependent launch (PDL) allowed: the kernel may
+// be scheduled while the previous kernel on the stream is finishing; every
+// kernel of this library calls pdl_wait() before it touches global memory,
+// so the overlap only hides launch latency and prologues.  Setting the
+// environment variable MOE_DISABLE_PDL=1 launches without the attribute.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(std::forward<Args>(args))...);
+}
+
 // ---------------------------------------------------------------- device side
+
+// Wait until the grids this one depends on have completed and their writes
+// are visible (a no-op when launched without PDL).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel on the stream to be scheduled (it still waits for
+// this grid's completion in its own pdl_wait()).
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 constexpr unsigned FULL = 0xffffffffu;
 

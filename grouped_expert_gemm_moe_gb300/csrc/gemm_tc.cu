@@ -24,6 +24,8 @@
 //    mode stores the accumulator as bf16.
 // Every mbarrier wait is bounded (1 s); on running out the kernel records
 // MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <stdlib.h>
+
 #include <algorithm>
 
 #include "tc_common.cuh"
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         prefetch_tmap(&tm_w);
     }
     if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
+    pdl_wait();       // predecessors' writes (offsets, activations) are visible after this
+    pdl_trigger();
     if (warp == 2) build_tile_table(offsets, G, M, n_tiles, s_off, s_tile, s_total, dev_error);
     tc_fence_before();
     __syncthreads();
@@ -269,7 +273,7 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
     static int attr_done[64] = {0};
     if (!raise_smem_limit(tc_grouped_gemm<SWIGLU, BN>, attr_done)) return MOE_ERR_CUDA;
-    tc_grouped_gemm<SWIGLU, BN><<<sm_count(), TC_THREADS, smem, stream>>>(
+    launch(tc_grouped_gemm<SWIGLU, BN>, sm_count(), TC_THREADS, smem, stream, 
         tm_act, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
 }
@@ -278,6 +282,30 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
 
 using namespace moe;
 
+// Weight rows per tile: 256 for large batches (fewer, larger MMAs), 128
+// when the groups are small (an average of <= 64 rows per group): the
+// launch then has twice as many tiles, which evens out the last wave of the
+// persistent grid.  MOE_GEMM_BN=128|256 in the environment overrides.
+static int pick_bn(int M, int G) {
+    static const int forced = [] {
+        const char *v = getenv("MOE_GEMM_BN");
+        return v ? atoi(v) : 0;
+    }();
+    if (forced == 128 || forced == 256) return forced;
+    return static_cast<int64_t>(M) <= 64ll * G ? 128 : 256;
+}
+
+template <bool SWIGLU>
+static moe_status launch_tc_bn(const void *act, const void *w, const int32_t *offsets, int G,
+                               int M, int K, int R, int NOUT, int UP_OFF, uint16_t *out,
+                               int32_t *dev_error, cudaStream_t stream) {
+    if (pick_bn(M, G) == 128)
+        return launch_tc<SWIGLU, 128>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,
+                                      stream);
+    return launch_tc<SWIGLU, 256>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,
+                                  stream);
+}
+
 extern "C" moe_status moe_grouped_gemm_gate_up(const uint16_t *x_perm, const int32_t *offsets,
                                                int G, int M, int H, int I, const uint16_t *w_gu,
                                                uint16_t *h, int32_t *dev_error,
@@ -285,7 +313,7 @@ extern "C" moe_status moe_grouped_gemm_gate_up(const uint16_t *x_perm, const int
     moe_status st = check_ffn_args(x_perm, offsets, G, M, H, I, w_gu, w_gu, h, h,
                                    moe_ffn_workspace_size(M, I), 8);
     if (st != MOE_OK) return st;
-    return launch_tc<true, 256>(x_perm, w_gu, offsets, G, M, H, 2 * I, I, I, h, dev_error, stream);
+    return launch_tc_bn<true>(x_perm, w_gu, offsets, G, M, H, 2 * I, I, I, h, dev_error, stream);
 }
 
 extern "C" moe_status moe_grouped_gemm_down(const uint16_t *h, const int32_t *offsets, int G,
@@ -295,7 +323,7 @@ extern "C" moe_status moe_grouped_gemm_down(const uint16_t *h, const int32_t *of
     moe_status st = check_ffn_args(h, offsets, G, M, H, I, w_down, w_down, y_perm, y_perm,
                                    moe_ffn_workspace_size(M, I), 8);
     if (st != MOE_OK) return st;
-    return launch_tc<false, 256>(h, w_down, offsets, G, M, I, H, H, 0, y_perm, dev_error, stream);
+    return launch_tc_bn<false>(h, w_down, offsets, G, M, I, H, H, 0, y_perm, dev_error, stream);
 }
 
 extern "C" moe_status moe_grouped_gemm_swiglu(const uint16_t *x_perm, const int32_t *offsets,
@@ -307,7 +335,7 @@ extern "C" moe_status moe_grouped_gemm_swiglu(const uint16_t *x_perm, const int3
                                    workspace_bytes, 8);
     if (st != MOE_OK) return st;
     uint16_t *h = static_cast<uint16_t *>(workspace);
-    st = launch_tc<true, 256>(x_perm, w_gu, offsets, G, M, H, 2 * I, I, I, h, dev_error, stream);
+    st = launch_tc_bn<true>(x_perm, w_gu, offsets, G, M, H, 2 * I, I, I, h, dev_error, stream);
     if (st != MOE_OK) return st;
-    return launch_tc<false, 256>(h, w_down, offsets, G, M, I, H, H, 0, y_perm, dev_error, stream);
+    return launch_tc_bn<false>(h, w_down, offsets, G, M, I, H, H, 0, y_perm, dev_error, stream);
 }

@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
         prefetch_tmap(&tm_q);
     }
     if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
+    pdl_wait();       // predecessors' writes (offsets, activations) are visible after this
+    pdl_trigger();
     if (warp == 2) build_tile_table(offsets, G, M, n_tiles, s_off, s_tile, s_total, dev_error);
     tc_fence_before();
     __syncthreads();
@@ -352,7 +354,7 @@ static moe_status launch_tc_w8(const void *act, const int8_t *q, const float *sc
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
     static int attr_done[64] = {0};
     if (!raise_smem_limit(tc_grouped_gemm_w8<SWIGLU>, attr_done)) return MOE_ERR_CUDA;
-    tc_grouped_gemm_w8<SWIGLU><<<sm_count(), W8_THREADS, smem, stream>>>(
+    launch(tc_grouped_gemm_w8<SWIGLU>, sm_count(), W8_THREADS, smem, stream, 
         tm_act, tm_q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
 }

@@ -94,6 +94,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_bf16(
     const uint16_t *__restrict__ x_perm, const int32_t *__restrict__ offsets, int G, int M, int H,
     int I, const uint16_t *__restrict__ w_gu, uint16_t *__restrict__ h, int32_t *dev_error) {
     __shared__ ActiveGroups ag;
+    pdl_wait();
+    pdl_trigger();
     const int na = load_active_groups(ag, offsets, G, M, dev_error);
     const int lane = lane_id(), wpb = blockDim.x >> 5;
     const int chunks = H / 8;
@@ -159,6 +161,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_bf16(
     int I, const uint16_t *__restrict__ w_down, uint16_t *__restrict__ y_perm,
     int32_t *dev_error) {
     __shared__ ActiveGroups ag;
+    pdl_wait();
+    pdl_trigger();
     const int na = load_active_groups(ag, offsets, G, M, dev_error);
     const int lane = lane_id(), wpb = blockDim.x >> 5;
     const int chunks = I / 8;
@@ -231,6 +235,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_w8(
     int I, const int8_t *__restrict__ q_gu, const float *__restrict__ s_gu,
     uint16_t *__restrict__ h, int32_t *dev_error) {
     __shared__ ActiveGroups ag;
+    pdl_wait();
+    pdl_trigger();
     const int na = load_active_groups(ag, offsets, G, M, dev_error);
     const int lane = lane_id(), wpb = blockDim.x >> 5;
     const int chunks = H / 16;                   // 16 int8 per 16-byte chunk
@@ -305,6 +311,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_w8(
     int I, const int8_t *__restrict__ q_down, const float *__restrict__ s_down,
     uint16_t *__restrict__ y_perm, int32_t *dev_error) {
     __shared__ ActiveGroups ag;
+    pdl_wait();
+    pdl_trigger();
     const int na = load_active_groups(ag, offsets, G, M, dev_error);
     const int lane = lane_id(), wpb = blockDim.x >> 5;
     const int chunks = I / 16;
@@ -382,46 +390,57 @@ static int pick_nch(int chunks) {            // chunks = 16-byte chunks per row
     return per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : 8;
 }
 
-static int gemv_blocks() { return sm_count() * 4; }
+// All blocks of a GEMV launch are resident at once (grid = blocks per SM x
+// SMs), so the grid-stride task loop never waits for a second wave.
+template <typename Kernel>
+static int resident_grid(Kernel kernel) {
+    static int per_sm_of_device[64] = {0};     // one cache per kernel instantiation
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (per_sm_of_device[dev] < 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, GEMV_THREADS, 0) !=
+                cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        per_sm_of_device[dev] = per_sm;
+    }
+    return per_sm_of_device[dev] * sm_count();
+}
 
 template <typename... A>
 static void launch_gateup_bf16(int nch, cudaStream_t s, A... a) {
-    const int b = gemv_blocks();
     switch (nch) {
-        case 1: gemv_gateup_bf16<1><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 2: gemv_gateup_bf16<2><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 4: gemv_gateup_bf16<4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        default: gemv_gateup_bf16<8><<<b, GEMV_THREADS, 0, s>>>(a...); break;
+        case 1: launch(gemv_gateup_bf16<1>, resident_grid(gemv_gateup_bf16<1>), GEMV_THREADS, 0, s, a...); break;
+        case 2: launch(gemv_gateup_bf16<2>, resident_grid(gemv_gateup_bf16<2>), GEMV_THREADS, 0, s, a...); break;
+        case 4: launch(gemv_gateup_bf16<4>, resident_grid(gemv_gateup_bf16<4>), GEMV_THREADS, 0, s, a...); break;
+        default: launch(gemv_gateup_bf16<8>, resident_grid(gemv_gateup_bf16<8>), GEMV_THREADS, 0, s, a...); break;
     }
 }
 template <typename... A>
 static void launch_down_bf16(int nch, cudaStream_t s, A... a) {
-    const int b = gemv_blocks();
     switch (nch) {
-        case 1: gemv_down_bf16<1, 4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 2: gemv_down_bf16<2, 4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 4: gemv_down_bf16<4, 4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        default: gemv_down_bf16<8, 2><<<b, GEMV_THREADS, 0, s>>>(a...); break;
+        case 1: launch(gemv_down_bf16<1, 4>, resident_grid(gemv_down_bf16<1, 4>), GEMV_THREADS, 0, s, a...); break;
+        case 2: launch(gemv_down_bf16<2, 4>, resident_grid(gemv_down_bf16<2, 4>), GEMV_THREADS, 0, s, a...); break;
+        case 4: launch(gemv_down_bf16<4, 4>, resident_grid(gemv_down_bf16<4, 4>), GEMV_THREADS, 0, s, a...); break;
+        default: launch(gemv_down_bf16<8, 2>, resident_grid(gemv_down_bf16<8, 2>), GEMV_THREADS, 0, s, a...); break;
     }
 }
 template <typename... A>
 static void launch_gateup_w8(int nch, cudaStream_t s, A... a) {
-    const int b = gemv_blocks();
     switch (nch) {
-        case 1: gemv_gateup_w8<1><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 2: gemv_gateup_w8<2><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 4: gemv_gateup_w8<4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        default: gemv_gateup_w8<8><<<b, GEMV_THREADS, 0, s>>>(a...); break;
+        case 1: launch(gemv_gateup_w8<1>, resident_grid(gemv_gateup_w8<1>), GEMV_THREADS, 0, s, a...); break;
+        case 2: launch(gemv_gateup_w8<2>, resident_grid(gemv_gateup_w8<2>), GEMV_THREADS, 0, s, a...); break;
+        case 4: launch(gemv_gateup_w8<4>, resident_grid(gemv_gateup_w8<4>), GEMV_THREADS, 0, s, a...); break;
+        default: launch(gemv_gateup_w8<8>, resident_grid(gemv_gateup_w8<8>), GEMV_THREADS, 0, s, a...); break;
     }
 }
 template <typename... A>
 static void launch_down_w8(int nch, cudaStream_t s, A... a) {
-    const int b = gemv_blocks();
     switch (nch) {
-        case 1: gemv_down_w8<1, 4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 2: gemv_down_w8<2, 4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        case 4: gemv_down_w8<4, 4><<<b, GEMV_THREADS, 0, s>>>(a...); break;
-        default: gemv_down_w8<8, 2><<<b, GEMV_THREADS, 0, s>>>(a...); break;
+        case 1: launch(gemv_down_w8<1, 4>, resident_grid(gemv_down_w8<1, 4>), GEMV_THREADS, 0, s, a...); break;
+        case 2: launch(gemv_down_w8<2, 4>, resident_grid(gemv_down_w8<2, 4>), GEMV_THREADS, 0, s, a...); break;
+        case 4: launch(gemv_down_w8<4, 4>, resident_grid(gemv_down_w8<4, 4>), GEMV_THREADS, 0, s, a...); break;
+        default: launch(gemv_down_w8<8, 2>, resident_grid(gemv_down_w8<8, 2>), GEMV_THREADS, 0, s, a...); break;
     }
 }
 

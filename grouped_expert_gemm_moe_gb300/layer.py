@@ -30,6 +30,7 @@ class LayerBuffers:
     x_perm: torch.Tensor
     y_perm: torch.Tensor
     ffn_ws: torch.Tensor
+    perm_ws: torch.Tensor | None
     out: torch.Tensor
 
 
@@ -67,6 +68,7 @@ class MoELayer:
             d = self.device
             M = self.rows(T)
             ws = B.moe_ffn_workspace_size(M, self.I)
+            pws = B.moe_permute_workspace_size(T, self.E, self.S, self.k)
             b = LayerBuffers(
                 T=T,
                 topk_ids=torch.empty((T, self.k), dtype=torch.int32, device=d),
@@ -77,6 +79,7 @@ class MoELayer:
                 x_perm=torch.empty((M, self.H), dtype=torch.bfloat16, device=d),
                 y_perm=torch.empty((M, self.H), dtype=torch.bfloat16, device=d),
                 ffn_ws=torch.empty(max(ws, 256), dtype=torch.uint8, device=d),
+                perm_ws=(torch.empty(pws, dtype=torch.uint8, device=d) if pws else None),
                 out=torch.empty((T, self.H), dtype=torch.bfloat16, device=d),
             )
             self._bufs[T] = b
@@ -90,7 +93,24 @@ class MoELayer:
 
     def permute(self, x, b: LayerBuffers, stream=None):
         B.moe_permute(b.topk_ids, self.E, self.S, x, b.offsets, b.sorted_slot, b.row_of_slot,
-                      b.x_perm, None, self.err, stream)
+                      b.x_perm, b.perm_ws, self.err, stream)
+
+    def fused_route_permute_ok(self, T: int) -> bool:
+        # the fused kernel routes every token in every CTA, one warp per token:
+        # worth it while a CTA's 32 warps route each token at most once
+        return (T <= 32 and T * self.k <= B.ROUTE_PERMUTE_MAX_SLOTS
+                and self.E <= B.ROUTE_PERMUTE_MAX_E)
+
+    def route_permute(self, logits, x, b: LayerBuffers, stream=None):
+        """Routing and permutation: one fused launch for decode-sized batches,
+        the two separate calls otherwise (identical results)."""
+        if self.fused_route_permute_ok(b.T):
+            B.moe_route_permute(logits, self.k, self.renormalize, self.S, x, b.topk_ids, b.topk_w,
+                                b.offsets, b.sorted_slot, b.row_of_slot, b.x_perm, self.err,
+                                stream)
+        else:
+            self.route(logits, b, stream)
+            self.permute(x, b, stream)
 
     def hidden(self, b: LayerBuffers) -> torch.Tensor:
         """The bf16 hidden rows h [M, I] inside the FFN workspace."""
@@ -124,8 +144,7 @@ class MoELayer:
         T = x.shape[0]
         b = self.buffers(T)
         kind = self.choose_ffn(T) if ffn == "auto" else ffn
-        self.route(logits, b, stream)
-        self.permute(x, b, stream)
+        self.route_permute(logits, x, b, stream)
         self.ffn(b, kind, stream)
         dst = b.out if out is None else out
         self.combine(b, dst, residual, stream)

@@ -96,7 +96,8 @@ moe_status moe_router_logits(const uint16_t *x, const uint16_t *w_r, const float
 moe_status moe_route(const float *logits, int T, int E, int k, int renormalize,
                      int32_t *topk_ids, float *topk_w, int32_t *dev_error, cudaStream_t stream);
 
-/* Workspace bytes moe_permute needs (currently 0: it works in shared memory). */
+/* Workspace bytes moe_permute needs: 0 for up to 1024 slots (T*k), else
+ * ceil(T*k / 1024) * (E + 1) int32 chunk counts, rounded up to 256. */
 size_t moe_permute_workspace_size(int T, int E, int S, int k);
 
 /*
@@ -114,12 +115,30 @@ size_t moe_permute_workspace_size(int T, int E, int S, int k);
  *   row_of_slot [T*k] int32: inverse of sorted_slot (-1 for a slot whose
  *               expert id was invalid).
  *   x_perm      [M,H] bf16: row r = x[token of row r].
- * An expert id outside [0,E) is a device-check fault; that slot is dropped.
+ * An expert id outside [0,E) is a device-check fault: every group is left
+ * empty and every row_of_slot entry -1.  workspace: device memory of at
+ * least moe_permute_workspace_size(T, E, S, k) bytes (4-byte aligned; NULL
+ * when that size is 0).
  */
 moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, int k, const void *x,
                        int x_dtype, int H, int32_t *offsets, int32_t *sorted_slot,
                        int32_t *row_of_slot, uint16_t *x_perm, void *workspace,
                        size_t workspace_bytes, int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * moe_route_permute -- moe_route followed by moe_permute in one launch, for
+ * decode-sized batches (T*k <= 1024 slots, E <= 256; otherwise
+ * MOE_ERR_UNSUPPORTED and nothing is launched).  Same arguments and the same
+ * outputs, bit for bit, as the two calls (no permute workspace is needed);
+ * a NaN logit is a device-check fault that leaves every group empty.  The
+ * pages route and sort in separate steps ("switchyard" page, "Route and
+ * sort"); fusing them removes a launch and a round trip through global
+ * memory from the latency-bound decode step.
+ */
+moe_status moe_route_permute(const float *logits, int T, int E, int S, int k, int renormalize,
+                             const void *x, int x_dtype, int H, int32_t *topk_ids, float *topk_w,
+                             int32_t *offsets, int32_t *sorted_slot, int32_t *row_of_slot,
+                             uint16_t *x_perm, int32_t *dev_error, cudaStream_t stream);
 
 /* Workspace bytes of the FFN calls below: the bf16 hidden rows h [M,I]. */
 size_t moe_ffn_workspace_size(int M, int I);

@@ -69,7 +69,9 @@ def test_workspace_sizes(lib):
     lib.moe_permute_workspace_size.restype = ctypes.c_size_t
     assert lib.moe_ffn_workspace_size(16384, 1024) == 16384 * 1024 * 2
     assert lib.moe_ffn_workspace_size(3, 8) == 256
-    assert lib.moe_permute_workspace_size(2048, 64, 2, 6) == 0
+    assert lib.moe_permute_workspace_size(128, 64, 2, 8) == 0          # <= 1024 slots
+    # 12288 slots: 12 chunks x (64 + 1) int32 counts, rounded up to 256 bytes
+    assert lib.moe_permute_workspace_size(2048, 64, 2, 6) == 3328
 
 
 P = ctypes.c_void_p

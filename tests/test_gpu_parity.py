@@ -212,9 +212,9 @@ def test_residual_and_aliasing(B, L):
     assert_close(to_np(buf), y, "residual")
 
 
-def test_invalid_expert_id_is_reported_without_out_of_bounds(B, L):
+@pytest.mark.parametrize("T", [10, 700])          # one chunk of slots / several chunks
+def test_invalid_expert_id_is_reported_without_out_of_bounds(B, L, T):
     sh = W.MoEShape("bad", H=64, E=8, k=2, I=64, S=1)
-    T = 10
     inp = W.make_layer(sh, T, "uniform", seed=4)
     layer = make_layer_obj(L, inp)
     b = layer.buffers(T)
@@ -278,3 +278,85 @@ def test_router_logits_kernel(B):
     got = out.cpu().numpy().astype(np.float64)
     # fp32 accumulation of 2048 products: error << 1e-4 of the logit scale
     assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+
+
+FUSED_CASES = [("tiny", 16, "uniform"), ("olmoe", 1, "uniform"), ("olmoe", 8, "uniform"),
+               ("olmoe", 64, "uniform"), ("deepseek", 16, "zipf"), ("deepseek", 128, "uniform")]
+
+
+@pytest.mark.parametrize("name,T,routing", FUSED_CASES)
+def test_fused_route_permute_bit_exact(B, L, name, T, routing):
+    """moe_route_permute gives the same bits as the oracle's route + permute."""
+    inp, h = layer_case(name, T, routing)
+    sh = inp.shape
+    layer = make_layer_obj(L, inp)
+    b = layer.buffers(T)
+    for t_ in (b.topk_ids, b.offsets, b.sorted_slot, b.row_of_slot):
+        t_.fill_(-7)
+    b.x_perm.zero_()
+    B.moe_route_permute(inp.logits.to(DEV), sh.k, sh.renormalize, sh.S, inp.x.to(DEV),
+                        b.topk_ids, b.topk_w, b.offsets, b.sorted_slot, b.row_of_slot, b.x_perm,
+                        layer.err)
+    layer.check()
+    ids_ref, w_ref = oracle.route(h["logits"], sh.k, sh.renormalize)
+    np.testing.assert_array_equal(b.topk_ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(b.topk_w.cpu().numpy().astype(np.float64), w_ref, rtol=W_RTOL)
+    off, ss, ros = oracle.permute(ids_ref, sh.E, sh.S)
+    np.testing.assert_array_equal(b.offsets.cpu().numpy(), off)
+    np.testing.assert_array_equal(b.sorted_slot.cpu().numpy(), ss)
+    np.testing.assert_array_equal(b.row_of_slot.cpu().numpy(), ros)
+    tok = np.concatenate([ss // sh.k] + [np.arange(T)] * sh.S)
+    xb = inp.x.to(torch.bfloat16).cpu()
+    assert torch.equal(b.x_perm.cpu(), xb[torch.from_numpy(tok).long()])
+
+
+def test_fused_route_permute_limits_and_nan(B, L):
+    inp, _ = layer_case("tiny", 16, "uniform")
+    sh = inp.shape
+    layer = make_layer_obj(L, inp)
+    b = layer.buffers(16)
+    logits = inp.logits.clone()
+    logits[5, 1] = float("nan")
+    B.moe_route_permute(logits.to(DEV), sh.k, sh.renormalize, sh.S, inp.x.to(DEV), b.topk_ids,
+                        b.topk_w, b.offsets, b.sorted_slot, b.row_of_slot, b.x_perm, layer.err)
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 6
+    assert (b.offsets.cpu() == 0).all() and (b.row_of_slot.cpu() == -1).all()
+    # beyond its limits the call refuses without launching
+    big = torch.zeros((600, 8), dtype=torch.float32, device=DEV)      # 600 * 2 > 1024 slots
+    with pytest.raises(B.MoEError):
+        B.moe_route_permute(big, 2, False, 0, torch.zeros((600, 256), dtype=torch.bfloat16,
+                                                          device=DEV),
+                            torch.empty((600, 2), dtype=torch.int32, device=DEV),
+                            torch.empty((600, 2), dtype=torch.float32, device=DEV),
+                            torch.empty(9, dtype=torch.int32, device=DEV),
+                            torch.empty(1200, dtype=torch.int32, device=DEV),
+                            torch.empty(1200, dtype=torch.int32, device=DEV),
+                            torch.empty((1200, 256), dtype=torch.bfloat16, device=DEV))
+
+
+@pytest.mark.parametrize("bn", ["128", "256"])
+def test_gemm_tile_widths_agree(B, L, bn, monkeypatch):
+    """Both tile widths of the tcgen05 GEMM give results within tolerance of
+    the oracle on a DeepSeek-shaped batch (the width is chosen per call)."""
+    import subprocess, sys, os
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "import numpy as np, torch, oracle\n"
+        "from grouped_expert_gemm_moe_gb300 import workloads as W\n"
+        "from grouped_expert_gemm_moe_gb300.layer import MoELayer\n"
+        "sys.path.insert(0, %r)\n"
+        "from gpu_helpers import host_inputs, oracle_out, sample_tokens, assert_close, to_np\n"
+        "inp = W.make_layer(W.DEEPSEEK, 512, 'zipf', seed=0, device='cuda:0')\n"
+        "h = host_inputs(inp); sh = inp.shape\n"
+        "ly = MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize, w_gu=inp.w_gu, w_down=inp.w_down, device='cuda:0')\n"
+        "out = ly.forward(inp.x, inp.logits, ffn='gemm'); ly.check()\n"
+        "tok = sample_tokens(512)\n"
+        "_, _, y = oracle_out(inp, h, tokens=tok)\n"
+        "print(assert_close(to_np(out)[tok], y, 'bn'))\n"
+    ) % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+         os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_GEMM_BN=bn)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
