@@ -51,6 +51,7 @@ struct TcCfg {
 template <bool SWIGLU, int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_act128,
                     const __grid_constant__ CUtensorMap tm_w, const int32_t *__restrict__ offsets,
                     int G, int M, int K, int R, int NOUT, int UP_OFF, uint16_t *__restrict__ out,
                     int32_t *dev_error) {
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_act128);
         prefetch_tmap(&tm_w);
     }
     if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
@@ -112,7 +114,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile(t, s_tile, s_off, G);
-                const int nbox = (ti.nrows + TC_ABOX - 1) / TC_ABOX;
+                // a tile with more than 64 rows takes one 128-row box; a smaller
+                // one only the 16-row boxes it needs (rows past the group are
+                // loaded but never stored)
+                const bool full_box = ti.nrows > 64;
+                const int nbox = full_box ? TC_BM / TC_ABOX : (ti.nrows + TC_ABOX - 1) / TC_ABOX;
                 const uint32_t bytes = nbox * TC_ABOX * TC_BK * 2 + C::B_BYTES;
                 const int wrow = ti.g * R + ti.nt * n_per_tile;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -124,9 +130,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     uint8_t *a = sA + stage * C::A_BYTES;
                     uint8_t *b = sB + stage * C::B_BYTES;
                     const int kx = kb * TC_BK;
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d(a + bx * TC_ABOX * 128, &tm_act, &full[stage], kx,
-                                    ti.m0 + bx * TC_ABOX, pol_a);
+                    if (full_box)
+                        tma_load_2d(a, &tm_act128, &full[stage], kx, ti.m0, pol_a);
+                    else
+                        for (int bx = 0; bx < nbox; ++bx)
+                            tma_load_2d(a + bx * TC_ABOX * 128, &tm_act, &full[stage], kx,
+                                        ti.m0 + bx * TC_ABOX, pol_a);
                     if (SWIGLU) {
                         tma_load_2d(b, &tm_w, &full[stage], kx, wrow, pol_w);
                         tma_load_2d(b + (BN / 2) * 128, &tm_w, &full[stage], kx, wrow + UP_OFF,
@@ -266,7 +275,9 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
                             int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
                             cudaStream_t stream) {
     CUtensorMap tm_act, tm_w;
+    CUtensorMap tm_act128;
     if (!encode_bf16_2d(&tm_act, act, K, M, TC_ABOX)) return MOE_ERR_CUDA;
+    if (!encode_bf16_2d(&tm_act128, act, K, M, TC_BM)) return MOE_ERR_CUDA;
     if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, SWIGLU ? BN / 2 : BN))
         return MOE_ERR_CUDA;
     const size_t smem = TcCfg<BN>::smem_bytes(G);
@@ -274,7 +285,7 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
     static int attr_done[64] = {0};
     if (!raise_smem_limit(tc_grouped_gemm<SWIGLU, BN>, attr_done)) return MOE_ERR_CUDA;
     launch(tc_grouped_gemm<SWIGLU, BN>, sm_count(), TC_THREADS, smem, stream, 
-        tm_act, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
+        tm_act, tm_act128, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
 }
 

@@ -63,6 +63,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 template <bool SWIGLU>
 __global__ void __launch_bounds__(W8_THREADS, 1)
     tc_grouped_gemm_w8(const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_act128,
                        const __grid_constant__ CUtensorMap tm_q, const float *__restrict__ scales,
                        const int32_t *__restrict__ offsets, int G, int M, int K, int R, int NOUT,
                        int UP_OFF, uint16_t *__restrict__ out, int32_t *dev_error) {
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_act128);
         prefetch_tmap(&tm_q);
     }
     if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
@@ -133,15 +135,22 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile(t, s_tile, s_off, G);
-                const int nbox = (ti.nrows + TC_ABOX - 1) / TC_ABOX;
+                // a tile with more than 64 rows takes one 128-row box; a smaller
+                // one only the 16-row boxes it needs (rows past the group are
+                // loaded but never stored)
+                const bool full_box = ti.nrows > 64;
+                const int nbox = full_box ? TC_BM / TC_ABOX : (ti.nrows + TC_ABOX - 1) / TC_ABOX;
                 const uint32_t bytes = nbox * TC_ABOX * TC_BK * 2;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&ab_empty[s], ph ^ 1u, dev_error)) { ok = false; break; }
                     mbar_arrive_expect_tx(&a_full[s], bytes);
                     uint8_t *a = sA + s * C::A_BYTES;
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d(a + bx * TC_ABOX * 128, &tm_act, &a_full[s], kb * TC_BK,
-                                    ti.m0 + bx * TC_ABOX, pol);
+                    if (full_box)
+                        tma_load_2d(a, &tm_act128, &a_full[s], kb * TC_BK, ti.m0, pol);
+                    else
+                        for (int bx = 0; bx < nbox; ++bx)
+                            tma_load_2d(a + bx * TC_ABOX * 128, &tm_act, &a_full[s], kb * TC_BK,
+                                        ti.m0 + bx * TC_ABOX, pol);
                     filled |= 1u << s;
                     fill_par = (fill_par & ~(1u << s)) | (ph << s);
                     if (++s == S) { s = 0; ph ^= 1u; }
@@ -347,7 +356,9 @@ static moe_status launch_tc_w8(const void *act, const int8_t *q, const float *sc
                                const int32_t *offsets, int G, int M, int K, int R, int NOUT,
                                int UP_OFF, uint16_t *out, int32_t *dev_error, cudaStream_t stream) {
     CUtensorMap tm_act, tm_q;
+    CUtensorMap tm_act128;
     if (!encode_bf16_2d(&tm_act, act, K, M, TC_ABOX)) return MOE_ERR_CUDA;
+    if (!encode_bf16_2d(&tm_act128, act, K, M, TC_BM)) return MOE_ERR_CUDA;
     if (!encode_u8_2d(&tm_q, q, K, static_cast<uint64_t>(G) * R, SWIGLU ? W8_BN / 2 : W8_BN))
         return MOE_ERR_CUDA;
     const size_t smem = W8Cfg::smem_bytes(G);
@@ -355,7 +366,7 @@ static moe_status launch_tc_w8(const void *act, const int8_t *q, const float *sc
     static int attr_done[64] = {0};
     if (!raise_smem_limit(tc_grouped_gemm_w8<SWIGLU>, attr_done)) return MOE_ERR_CUDA;
     launch(tc_grouped_gemm_w8<SWIGLU>, sm_count(), W8_THREADS, smem, stream, 
-        tm_act, tm_q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
+        tm_act, tm_act128, tm_q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
 }
 

@@ -88,8 +88,13 @@ __device__ __forceinline__ void unpack16_s8(const uint4 v, float (&f)[16]) {
 }
 
 // ------------------------------------------------------------------ bf16
+//
+// A task's loads -- the weight rows' chunks and the NR activation rows'
+// chunks this lane needs -- are all issued before the first multiply, so
+// one memory latency covers the whole task.  NR (1 or 2) is the number of
+// a group's rows handled per pass, picked from the average rows per group.
 
-template <int NCH>
+template <int NCH, int NR>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_bf16(
     const uint16_t *__restrict__ x_perm, const int32_t *__restrict__ offsets, int G, int M, int H,
     int I, const uint16_t *__restrict__ w_gu, uint16_t *__restrict__ h, int32_t *dev_error) {
@@ -106,33 +111,36 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_bf16(
         const int g = ag.group[a], r0 = ag.row0[a], nr = ag.nrows[a];
         const uint16_t *wg = w_gu + (static_cast<int64_t>(g) * 2 * I + i) * H;
         const uint16_t *wu = wg + static_cast<int64_t>(I) * H;
-        for (int rb = 0; rb < nr; rb += GEMV_NR) {
-            const int nrr = min(GEMV_NR, nr - rb);
-            float sg[GEMV_NR], su[GEMV_NR];
+        for (int rb = 0; rb < nr; rb += NR) {
+            const int nrr = min(NR, nr - rb);
+            const uint16_t *xr = x_perm + static_cast<int64_t>(r0 + rb) * H;
+            float sg[NR], su[NR];
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r) sg[r] = su[r] = 0.f;
+            for (int r = 0; r < NR; ++r) sg[r] = su[r] = 0.f;
             for (int seg = 0; seg < chunks; seg += 32 * NCH) {
-                uint4 vg[NCH], vu[NCH];
+                uint4 vg[NCH], vu[NCH], vx[NR][NCH];
 #pragma unroll
                 for (int u = 0; u < NCH; ++u) {
                     const int q = seg + lane + 32 * u;
                     if (q < chunks) {
                         vg[u] = ld_stream(wg + q * 8);
                         vu[u] = ld_stream(wu + q * 8);
+#pragma unroll
+                        for (int r = 0; r < NR; ++r)
+                            if (r < nrr) vx[r][u] = ld_nc(xr + static_cast<int64_t>(r) * H + q * 8);
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < NCH; ++u) {
-                    const int q = seg + lane + 32 * u;
-                    if (q >= chunks) continue;
+                    if (seg + lane + 32 * u >= chunks) continue;
                     float fg[8], fu[8];
                     unpack8(vg[u], fg);
                     unpack8(vu[u], fu);
 #pragma unroll
-                    for (int r = 0; r < GEMV_NR; ++r) {
+                    for (int r = 0; r < NR; ++r) {
                         if (r >= nrr) break;
                         float fx[8];
-                        unpack8(ld_nc(x_perm + static_cast<int64_t>(r0 + rb + r) * H + q * 8), fx);
+                        unpack8(vx[r][u], fx);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             sg[r] = fmaf(fg[e], fx[e], sg[r]);
@@ -142,7 +150,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_bf16(
                 }
             }
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 if (r >= nrr) break;
                 const float gv = warp_sum(sg[r]), uv = warp_sum(su[r]);
                 if (lane == 0) {
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_bf16(
     }
 }
 
-template <int NCH, int RW>
+template <int NCH, int RW, int NR>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_bf16(
     const uint16_t *__restrict__ h, const int32_t *__restrict__ offsets, int G, int M, int H,
     int I, const uint16_t *__restrict__ w_down, uint16_t *__restrict__ y_perm,
@@ -173,32 +181,36 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_bf16(
         const int a = static_cast<int>(task / nblk), n0 = static_cast<int>(task % nblk) * RW;
         const int g = ag.group[a], r0 = ag.row0[a], nr = ag.nrows[a];
         const uint16_t *wd = w_down + (static_cast<int64_t>(g) * H + n0) * I;
-        for (int rb = 0; rb < nr; rb += GEMV_NR) {
-            const int nrr = min(GEMV_NR, nr - rb);
-            float acc[GEMV_NR][RW];
+        for (int rb = 0; rb < nr; rb += NR) {
+            const int nrr = min(NR, nr - rb);
+            const uint16_t *hr = h + static_cast<int64_t>(r0 + rb) * I;
+            float acc[NR][RW];
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r)
+            for (int r = 0; r < NR; ++r)
 #pragma unroll
                 for (int w = 0; w < RW; ++w) acc[r][w] = 0.f;
             for (int seg = 0; seg < chunks; seg += 32 * NCH) {
-                uint4 vw[RW][NCH];
-#pragma unroll
-                for (int w = 0; w < RW; ++w)
-#pragma unroll
-                    for (int u = 0; u < NCH; ++u) {
-                        const int q = seg + lane + 32 * u;
-                        if (q < chunks && n0 + w < H)
-                            vw[w][u] = ld_stream(wd + static_cast<int64_t>(w) * I + q * 8);
-                    }
+                uint4 vw[RW][NCH], vx[NR][NCH];
 #pragma unroll
                 for (int u = 0; u < NCH; ++u) {
                     const int q = seg + lane + 32 * u;
-                    if (q >= chunks) continue;
+                    if (q < chunks) {
 #pragma unroll
-                    for (int r = 0; r < GEMV_NR; ++r) {
+                        for (int w = 0; w < RW; ++w)
+                            if (n0 + w < H) vw[w][u] = ld_stream(wd + static_cast<int64_t>(w) * I + q * 8);
+#pragma unroll
+                        for (int r = 0; r < NR; ++r)
+                            if (r < nrr) vx[r][u] = ld_nc(hr + static_cast<int64_t>(r) * I + q * 8);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < NCH; ++u) {
+                    if (seg + lane + 32 * u >= chunks) continue;
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) {
                         if (r >= nrr) break;
                         float fx[8];
-                        unpack8(ld_nc(h + static_cast<int64_t>(r0 + rb + r) * I + q * 8), fx);
+                        unpack8(vx[r][u], fx);
 #pragma unroll
                         for (int w = 0; w < RW; ++w) {
                             if (n0 + w >= H) break;
@@ -211,7 +223,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_bf16(
                 }
             }
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 if (r >= nrr) break;
 #pragma unroll
                 for (int w = 0; w < RW; ++w) {
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_bf16(
 
 // ------------------------------------------------------------------ int8
 
-template <int NCH>
+template <int NCH, int NR>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_w8(
     const uint16_t *__restrict__ x_perm, const int32_t *__restrict__ offsets, int G, int M, int H,
     int I, const int8_t *__restrict__ q_gu, const float *__restrict__ s_gu,
@@ -249,35 +261,40 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_w8(
         const int8_t *wu = wg + static_cast<int64_t>(I) * H;
         const float scg = s_gu[static_cast<int64_t>(g) * 2 * I + i];
         const float scu = s_gu[static_cast<int64_t>(g) * 2 * I + I + i];
-        for (int rb = 0; rb < nr; rb += GEMV_NR) {
-            const int nrr = min(GEMV_NR, nr - rb);
-            float sg[GEMV_NR], su[GEMV_NR];
+        for (int rb = 0; rb < nr; rb += NR) {
+            const int nrr = min(NR, nr - rb);
+            const uint16_t *xr = x_perm + static_cast<int64_t>(r0 + rb) * H;
+            float sg[NR], su[NR];
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r) sg[r] = su[r] = 0.f;
+            for (int r = 0; r < NR; ++r) sg[r] = su[r] = 0.f;
             for (int seg = 0; seg < chunks; seg += 32 * NCH) {
-                uint4 vg[NCH], vu[NCH];
+                uint4 vg[NCH], vu[NCH], vx[NR][NCH][2];
 #pragma unroll
                 for (int u = 0; u < NCH; ++u) {
                     const int q = seg + lane + 32 * u;
                     if (q < chunks) {
                         vg[u] = ld_stream(wg + q * 16);
                         vu[u] = ld_stream(wu + q * 16);
+#pragma unroll
+                        for (int r = 0; r < NR; ++r)
+                            if (r < nrr) {
+                                vx[r][u][0] = ld_nc(xr + static_cast<int64_t>(r) * H + q * 16);
+                                vx[r][u][1] = ld_nc(xr + static_cast<int64_t>(r) * H + q * 16 + 8);
+                            }
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < NCH; ++u) {
-                    const int q = seg + lane + 32 * u;
-                    if (q >= chunks) continue;
+                    if (seg + lane + 32 * u >= chunks) continue;
                     float fg[16], fu[16];
                     unpack16_s8(vg[u], fg);
                     unpack16_s8(vu[u], fu);
 #pragma unroll
-                    for (int r = 0; r < GEMV_NR; ++r) {
+                    for (int r = 0; r < NR; ++r) {
                         if (r >= nrr) break;
-                        const uint16_t *xr = x_perm + static_cast<int64_t>(r0 + rb + r) * H + q * 16;
                         float fx0[8], fx1[8];
-                        unpack8(ld_nc(xr), fx0);
-                        unpack8(ld_nc(xr + 8), fx1);
+                        unpack8(vx[r][u][0], fx0);
+                        unpack8(vx[r][u][1], fx1);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             sg[r] = fmaf(fg[e], fx0[e], sg[r]);
@@ -292,7 +309,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_w8(
                 }
             }
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 if (r >= nrr) break;
                 const float gv = warp_sum(sg[r]) * scg, uv = warp_sum(su[r]) * scu;
                 if (lane == 0) {
@@ -305,7 +322,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_w8(
     }
 }
 
-template <int NCH, int RW>
+template <int NCH, int RW, int NR>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_w8(
     const uint16_t *__restrict__ h, const int32_t *__restrict__ offsets, int G, int M, int H,
     int I, const int8_t *__restrict__ q_down, const float *__restrict__ s_down,
@@ -323,34 +340,40 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_w8(
         const int a = static_cast<int>(task / nblk), n0 = static_cast<int>(task % nblk) * RW;
         const int g = ag.group[a], r0 = ag.row0[a], nr = ag.nrows[a];
         const int8_t *wd = q_down + (static_cast<int64_t>(g) * H + n0) * I;
-        for (int rb = 0; rb < nr; rb += GEMV_NR) {
-            const int nrr = min(GEMV_NR, nr - rb);
-            float acc[GEMV_NR][RW];
+        for (int rb = 0; rb < nr; rb += NR) {
+            const int nrr = min(NR, nr - rb);
+            const uint16_t *hr = h + static_cast<int64_t>(r0 + rb) * I;
+            float acc[NR][RW];
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r)
+            for (int r = 0; r < NR; ++r)
 #pragma unroll
                 for (int w = 0; w < RW; ++w) acc[r][w] = 0.f;
             for (int seg = 0; seg < chunks; seg += 32 * NCH) {
-                uint4 vw[RW][NCH];
-#pragma unroll
-                for (int w = 0; w < RW; ++w)
-#pragma unroll
-                    for (int u = 0; u < NCH; ++u) {
-                        const int q = seg + lane + 32 * u;
-                        if (q < chunks && n0 + w < H)
-                            vw[w][u] = ld_stream(wd + static_cast<int64_t>(w) * I + q * 16);
-                    }
+                uint4 vw[RW][NCH], vx[NR][NCH][2];
 #pragma unroll
                 for (int u = 0; u < NCH; ++u) {
                     const int q = seg + lane + 32 * u;
-                    if (q >= chunks) continue;
+                    if (q < chunks) {
 #pragma unroll
-                    for (int r = 0; r < GEMV_NR; ++r) {
+                        for (int w = 0; w < RW; ++w)
+                            if (n0 + w < H) vw[w][u] = ld_stream(wd + static_cast<int64_t>(w) * I + q * 16);
+#pragma unroll
+                        for (int r = 0; r < NR; ++r)
+                            if (r < nrr) {
+                                vx[r][u][0] = ld_nc(hr + static_cast<int64_t>(r) * I + q * 16);
+                                vx[r][u][1] = ld_nc(hr + static_cast<int64_t>(r) * I + q * 16 + 8);
+                            }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < NCH; ++u) {
+                    if (seg + lane + 32 * u >= chunks) continue;
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) {
                         if (r >= nrr) break;
-                        const uint16_t *hr = h + static_cast<int64_t>(r0 + rb + r) * I + q * 16;
                         float fx0[8], fx1[8];
-                        unpack8(ld_nc(hr), fx0);
-                        unpack8(ld_nc(hr + 8), fx1);
+                        unpack8(vx[r][u][0], fx0);
+                        unpack8(vx[r][u][1], fx1);
 #pragma unroll
                         for (int w = 0; w < RW; ++w) {
                             if (n0 + w >= H) break;
@@ -366,7 +389,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_w8(
                 }
             }
 #pragma unroll
-            for (int r = 0; r < GEMV_NR; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 if (r >= nrr) break;
 #pragma unroll
                 for (int w = 0; w < RW; ++w) {
@@ -390,6 +413,10 @@ static int pick_nch(int chunks) {            // chunks = 16-byte chunks per row
     return per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : 8;
 }
 
+// rows per pass from the mean rows per group (M / G): 1, else 2 (groups
+// with more rows take several passes over the weight row, from L2)
+static int pick_nr(int M, int G) { return 2 * static_cast<int64_t>(M) <= 3ll * G ? 1 : 2; }
+
 // All blocks of a GEMV launch are resident at once (grid = blocks per SM x
 // SMs), so the grid-stride task loop never waits for a second wave.
 template <typename Kernel>
@@ -407,43 +434,54 @@ static int resident_grid(Kernel kernel) {
     return per_sm_of_device[dev] * sm_count();
 }
 
-template <typename... A>
-static void launch_gateup_bf16(int nch, cudaStream_t s, A... a) {
-    switch (nch) {
-        case 1: launch(gemv_gateup_bf16<1>, resident_grid(gemv_gateup_bf16<1>), GEMV_THREADS, 0, s, a...); break;
-        case 2: launch(gemv_gateup_bf16<2>, resident_grid(gemv_gateup_bf16<2>), GEMV_THREADS, 0, s, a...); break;
-        case 4: launch(gemv_gateup_bf16<4>, resident_grid(gemv_gateup_bf16<4>), GEMV_THREADS, 0, s, a...); break;
-        default: launch(gemv_gateup_bf16<8>, resident_grid(gemv_gateup_bf16<8>), GEMV_THREADS, 0, s, a...); break;
-    }
-}
-template <typename... A>
-static void launch_down_bf16(int nch, cudaStream_t s, A... a) {
-    switch (nch) {
-        case 1: launch(gemv_down_bf16<1, 4>, resident_grid(gemv_down_bf16<1, 4>), GEMV_THREADS, 0, s, a...); break;
-        case 2: launch(gemv_down_bf16<2, 4>, resident_grid(gemv_down_bf16<2, 4>), GEMV_THREADS, 0, s, a...); break;
-        case 4: launch(gemv_down_bf16<4, 4>, resident_grid(gemv_down_bf16<4, 4>), GEMV_THREADS, 0, s, a...); break;
-        default: launch(gemv_down_bf16<8, 2>, resident_grid(gemv_down_bf16<8, 2>), GEMV_THREADS, 0, s, a...); break;
-    }
-}
-template <typename... A>
-static void launch_gateup_w8(int nch, cudaStream_t s, A... a) {
-    switch (nch) {
-        case 1: launch(gemv_gateup_w8<1>, resident_grid(gemv_gateup_w8<1>), GEMV_THREADS, 0, s, a...); break;
-        case 2: launch(gemv_gateup_w8<2>, resident_grid(gemv_gateup_w8<2>), GEMV_THREADS, 0, s, a...); break;
-        case 4: launch(gemv_gateup_w8<4>, resident_grid(gemv_gateup_w8<4>), GEMV_THREADS, 0, s, a...); break;
-        default: launch(gemv_gateup_w8<8>, resident_grid(gemv_gateup_w8<8>), GEMV_THREADS, 0, s, a...); break;
-    }
-}
-template <typename... A>
-static void launch_down_w8(int nch, cudaStream_t s, A... a) {
-    switch (nch) {
-        case 1: launch(gemv_down_w8<1, 4>, resident_grid(gemv_down_w8<1, 4>), GEMV_THREADS, 0, s, a...); break;
-        case 2: launch(gemv_down_w8<2, 4>, resident_grid(gemv_down_w8<2, 4>), GEMV_THREADS, 0, s, a...); break;
-        case 4: launch(gemv_down_w8<4, 4>, resident_grid(gemv_down_w8<4, 4>), GEMV_THREADS, 0, s, a...); break;
-        default: launch(gemv_down_w8<8, 2>, resident_grid(gemv_down_w8<8, 2>), GEMV_THREADS, 0, s, a...); break;
-    }
+template <typename Kernel, typename... A>
+static void launch_resident(Kernel kernel, cudaStream_t s, A... a) {
+    launch(kernel, resident_grid(kernel), GEMV_THREADS, 0, s, a...);
 }
 
+#define MOE_GEMV_NR(KERNEL, NR_, ...)                                     \
+    switch (NR_) {                                                        \
+        case 1: launch_resident(KERNEL<__VA_ARGS__, 1>, s, a...); break;  \
+        default: launch_resident(KERNEL<__VA_ARGS__, 2>, s, a...); break; \
+    }
+
+template <typename... A>
+static void launch_gateup_bf16(int nch, int nr, cudaStream_t s, A... a) {
+    switch (nch) {
+        case 1: MOE_GEMV_NR(gemv_gateup_bf16, nr, 1); break;
+        case 2: MOE_GEMV_NR(gemv_gateup_bf16, nr, 2); break;
+        case 4: MOE_GEMV_NR(gemv_gateup_bf16, nr, 4); break;
+        default: MOE_GEMV_NR(gemv_gateup_bf16, nr, 8); break;
+    }
+}
+template <typename... A>
+static void launch_down_bf16(int nch, int nr, cudaStream_t s, A... a) {
+    switch (nch) {
+        case 1: MOE_GEMV_NR(gemv_down_bf16, nr, 1, 4); break;
+        case 2: MOE_GEMV_NR(gemv_down_bf16, nr, 2, 4); break;
+        case 4: MOE_GEMV_NR(gemv_down_bf16, nr, 4, 4); break;
+        default: MOE_GEMV_NR(gemv_down_bf16, nr, 8, 2); break;
+    }
+}
+template <typename... A>
+static void launch_gateup_w8(int nch, int nr, cudaStream_t s, A... a) {
+    switch (nch) {
+        case 1: MOE_GEMV_NR(gemv_gateup_w8, nr, 1); break;
+        case 2: MOE_GEMV_NR(gemv_gateup_w8, nr, 2); break;
+        case 4: MOE_GEMV_NR(gemv_gateup_w8, nr, 4); break;
+        default: MOE_GEMV_NR(gemv_gateup_w8, nr, 8); break;
+    }
+}
+template <typename... A>
+static void launch_down_w8(int nch, int nr, cudaStream_t s, A... a) {
+    switch (nch) {
+        case 1: MOE_GEMV_NR(gemv_down_w8, nr, 1, 4); break;
+        case 2: MOE_GEMV_NR(gemv_down_w8, nr, 2, 4); break;
+        case 4: MOE_GEMV_NR(gemv_down_w8, nr, 4, 4); break;
+        default: MOE_GEMV_NR(gemv_down_w8, nr, 8, 2); break;
+    }
+}
+#undef MOE_GEMV_NR
 }  // namespace moe
 
 using namespace moe;
@@ -495,7 +533,7 @@ extern "C" moe_status moe_grouped_gemv_gate_up(const uint16_t *x_perm, const int
                                                cudaStream_t stream) {
     moe_status st = check_phase_args(x_perm, offsets, G, M, H, I, w_gu, h, 8);
     if (st != MOE_OK) return st;
-    launch_gateup_bf16(pick_nch(H / 8), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
+    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
     return launch_status();
 }
 
@@ -505,7 +543,7 @@ extern "C" moe_status moe_grouped_gemv_down(const uint16_t *h, const int32_t *of
                                             cudaStream_t stream) {
     moe_status st = check_phase_args(h, offsets, G, M, H, I, w_down, y_perm, 8);
     if (st != MOE_OK) return st;
-    launch_down_bf16(pick_nch(I / 8), stream, h, offsets, G, M, H, I, w_down, y_perm, dev_error);
+    launch_down_bf16(pick_nch(I / 8), pick_nr(M, G), stream, h, offsets, G, M, H, I, w_down, y_perm, dev_error);
     return launch_status();
 }
 
@@ -518,9 +556,9 @@ extern "C" moe_status moe_grouped_gemv(const uint16_t *x_perm, const int32_t *of
                                    workspace_bytes, 8);
     if (st != MOE_OK) return st;
     uint16_t *h = static_cast<uint16_t *>(workspace);
-    launch_gateup_bf16(pick_nch(H / 8), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
+    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
     if ((st = launch_status()) != MOE_OK) return st;
-    launch_down_bf16(pick_nch(I / 8), stream, static_cast<const uint16_t *>(h), offsets, G, M, H, I,
+    launch_down_bf16(pick_nch(I / 8), pick_nr(M, G), stream, static_cast<const uint16_t *>(h), offsets, G, M, H, I,
                      w_down, y_perm, dev_error);
     return launch_status();
 }
@@ -536,10 +574,10 @@ extern "C" moe_status moe_grouped_gemv_w8(const uint16_t *x_perm, const int32_t 
     if (st != MOE_OK) return st;
     if (!s_gu || !s_down) return MOE_ERR_INVALID_ARG;
     uint16_t *h = static_cast<uint16_t *>(workspace);
-    launch_gateup_w8(pick_nch(H / 16), stream, x_perm, offsets, G, M, H, I, q_gu, s_gu, h,
+    launch_gateup_w8(pick_nch(H / 16), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, q_gu, s_gu, h,
                      dev_error);
     if ((st = launch_status()) != MOE_OK) return st;
-    launch_down_w8(pick_nch(I / 16), stream, static_cast<const uint16_t *>(h), offsets, G, M, H, I,
+    launch_down_w8(pick_nch(I / 16), pick_nr(M, G), stream, static_cast<const uint16_t *>(h), offsets, G, M, H, I,
                    q_down, s_down, y_perm, dev_error);
     return launch_status();
 }
@@ -601,9 +639,9 @@ extern "C" moe_status moe_grouped_gemv_noalloc(const uint16_t *x_perm, const int
     if (h == nullptr) return st;
     // Nothing in the scratch has to start at zero: the gate/up pass writes
     // every h row of every non-empty group before the down pass reads it.
-    launch_gateup_bf16(pick_nch(H / 8), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
+    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
     if ((st = launch_status()) != MOE_OK) return st;
-    launch_down_bf16(pick_nch(I / 8), stream, static_cast<const uint16_t *>(h), offsets, G, M, H,
+    launch_down_bf16(pick_nch(I / 8), pick_nr(M, G), stream, static_cast<const uint16_t *>(h), offsets, G, M, H,
                      I, w_down, y_perm, dev_error);
     return launch_status();
 }
