@@ -10,6 +10,8 @@
 
 namespace moe {
 
+constexpr int CB_CPT = 2;             // 8-element chunks per thread
+
 __global__ void __launch_bounds__(256) combine_kernel(
     const uint16_t *__restrict__ y_perm, const int32_t *__restrict__ row_of_slot,
     const float *__restrict__ topk_w, int T, int k, int S, int H,
@@ -17,26 +19,27 @@ __global__ void __launch_bounds__(256) combine_kernel(
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.y;
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;     // 8-element chunk
-    if (c * 8 >= H) return;
+    const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * CB_CPT;   // first chunk
+    const int chunks = H / 8;
+    if (c0 >= chunks) return;
     const int64_t n = static_cast<int64_t>(T) * k;
-    float acc[8];
+    float acc[CB_CPT][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-
-    // issue the loads of up to 8 routed rows at once (their indices and
-    // weights first, then the rows), so the gathers overlap instead of
-    // paying one memory latency per expert in turn; sums stay in j order
-    constexpr int BATCH = 8;
-    auto accumulate = [&](const uint4 &v, float w) {
+    for (int q = 0; q < CB_CPT; ++q)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+    auto accumulate = [&](int q, const uint4 &v, float w) {
         const uint32_t p[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(w, bf_lo(p[i]), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(w, bf_hi(p[i]), acc[2 * i + 1]);
+            acc[q][2 * i] = fmaf(w, bf_lo(p[i]), acc[q][2 * i]);
+            acc[q][2 * i + 1] = fmaf(w, bf_hi(p[i]), acc[q][2 * i + 1]);
         }
     };
-    for (int j0 = 0; j0 < k; j0 += BATCH) {              // routed rows, j ascending
+    // up to 8 routed rows at a time: their indices and weights first, then
+    // every row's chunks, so the gathers overlap; sums stay in j order
+    constexpr int BATCH = 8;
+    for (int j0 = 0; j0 < k; j0 += BATCH) {
         int64_t r[BATCH];
         float w[BATCH];
         bool ok[BATCH];
@@ -51,38 +54,53 @@ __global__ void __launch_bounds__(256) combine_kernel(
                 if (!ok[j]) report(dev_error, MOE_ERR_DEVICE_CHECK);
             }
         }
-        uint4 v[BATCH];
+        uint4 v[BATCH][CB_CPT];
 #pragma unroll
         for (int j = 0; j < BATCH; ++j)
-            if (ok[j]) v[j] = ld_nc(y_perm + r[j] * H + c * 8);
+#pragma unroll
+            for (int q = 0; q < CB_CPT; ++q)
+                if (ok[j] && c0 + q < chunks) v[j][q] = ld_nc(y_perm + r[j] * H + (c0 + q) * 8);
 #pragma unroll
         for (int j = 0; j < BATCH; ++j)
-            if (ok[j]) accumulate(v[j], w[j]);
+#pragma unroll
+            for (int q = 0; q < CB_CPT; ++q)
+                if (ok[j] && c0 + q < chunks) accumulate(q, v[j][q], w[j]);
     }
     for (int s0 = 0; s0 < S; s0 += BATCH) {              // shared rows, s ascending
-        uint4 v[BATCH];
+        uint4 v[BATCH][CB_CPT];
 #pragma unroll
         for (int j = 0; j < BATCH; ++j)
-            if (s0 + j < S) v[j] = ld_nc(y_perm + (n + static_cast<int64_t>(s0 + j) * T + t) * H + c * 8);
+#pragma unroll
+            for (int q = 0; q < CB_CPT; ++q)
+                if (s0 + j < S && c0 + q < chunks)
+                    v[j][q] = ld_nc(y_perm + (n + static_cast<int64_t>(s0 + j) * T + t) * H +
+                                    (c0 + q) * 8);
 #pragma unroll
         for (int j = 0; j < BATCH; ++j)
-            if (s0 + j < S) accumulate(v[j], 1.0f);
+#pragma unroll
+            for (int q = 0; q < CB_CPT; ++q)
+                if (s0 + j < S && c0 + q < chunks) accumulate(q, v[j][q], 1.0f);
     }
-    if (residual) {
-        const uint4 v = ld_nc(residual + static_cast<int64_t>(t) * H + c * 8);
-        const uint32_t p[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] += bf_lo(p[i]);
-            acc[2 * i + 1] += bf_hi(p[i]);
+    for (int q = 0; q < CB_CPT; ++q) {
+        const int c = c0 + q;
+        if (c >= chunks) break;
+        if (residual) {
+            const uint4 v = ld_nc(residual + static_cast<int64_t>(t) * H + c * 8);
+            const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[q][2 * i] += bf_lo(p[i]);
+                acc[q][2 * i + 1] += bf_hi(p[i]);
+            }
         }
+        uint4 o;
+        o.x = pack_bf16x2(acc[q][0], acc[q][1]);
+        o.y = pack_bf16x2(acc[q][2], acc[q][3]);
+        o.z = pack_bf16x2(acc[q][4], acc[q][5]);
+        o.w = pack_bf16x2(acc[q][6], acc[q][7]);
+        *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(t) * H + c * 8) = o;
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(t) * H + c * 8) = o;
 }
 
 }  // namespace moe
@@ -101,8 +119,9 @@ extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_
         return MOE_ERR_ALIGNMENT;
     if (T > 65535) return MOE_ERR_UNSUPPORTED;   // grid.y limit
     const int chunks = H / 8;
-    const int threads = chunks >= 256 ? 256 : ((chunks + 31) / 32) * 32;
-    dim3 grid((chunks + threads - 1) / threads, T);
+    const int per_thread = (chunks + CB_CPT - 1) / CB_CPT;
+    const int threads = per_thread >= 128 ? 128 : ((per_thread + 31) / 32) * 32;
+    dim3 grid((per_thread + threads - 1) / threads, T);
     launch(combine_kernel, grid, threads, 0, stream, y_perm, row_of_slot, topk_w, T, k, S, H, residual,
                                                  out, dev_error);
     return launch_status();

@@ -25,6 +25,7 @@
 // Every mbarrier wait is bounded (1 s); on running out the kernel records
 // MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 
@@ -293,28 +294,53 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
 
 using namespace moe;
 
-// Weight rows per tile: 256 for large batches (fewer, larger MMAs), 128
-// when the groups are small (an average of <= 64 rows per group): the
-// launch then has twice as many tiles, which evens out the last wave of the
-// persistent grid.  MOE_GEMM_BN=128|256 in the environment overrides.
-static int pick_bn(int M, int G) {
+namespace moe {
+template <bool SWIGLU>
+moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, int G, int M,
+                        int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
+                        cudaStream_t stream);
+}  // namespace moe
+
+// Tile shape per call, from the mean rows per group (M / G):
+//   <= 64 rows : 128 x 128 tiles (twice the tiles of 128 x 256, which evens
+//                out the last wave when the groups are small);
+//   <= 512 rows: 128 x 256 tiles;
+//   more       : 256-row token blocks x 256 weight rows (gemm_tc256.cu), which
+//                need a third fewer operand bytes per FLOP and win once most
+//                groups fill several blocks (measured on GB300: 0.73 of bf16
+//                peak at 1024 rows per group against 0.65 for 128 x 256).
+// MOE_GEMM_TILE=128|256|prefill in the environment overrides the choice.
+enum { TILE_128 = 0, TILE_256 = 1, TILE_PREFILL = 2 };
+static int pick_tile(int M, int G) {
     static const int forced = [] {
-        const char *v = getenv("MOE_GEMM_BN");
-        return v ? atoi(v) : 0;
+        const char *v = getenv("MOE_GEMM_TILE");
+        if (!v) return -1;
+        if (!strcmp(v, "128")) return static_cast<int>(TILE_128);
+        if (!strcmp(v, "256")) return static_cast<int>(TILE_256);
+        if (!strcmp(v, "prefill")) return static_cast<int>(TILE_PREFILL);
+        return -1;
     }();
-    if (forced == 128 || forced == 256) return forced;
-    return static_cast<int64_t>(M) <= 64ll * G ? 128 : 256;
+    if (forced >= 0) return forced;
+    if (static_cast<int64_t>(M) <= 64ll * G) return TILE_128;
+    if (static_cast<int64_t>(M) <= 512ll * G) return TILE_256;
+    return TILE_PREFILL;
 }
 
 template <bool SWIGLU>
 static moe_status launch_tc_bn(const void *act, const void *w, const int32_t *offsets, int G,
                                int M, int K, int R, int NOUT, int UP_OFF, uint16_t *out,
                                int32_t *dev_error, cudaStream_t stream) {
-    if (pick_bn(M, G) == 128)
-        return launch_tc<SWIGLU, 128>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,
-                                      stream);
-    return launch_tc<SWIGLU, 256>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,
-                                  stream);
+    switch (pick_tile(M, G)) {
+        case TILE_128:
+            return launch_tc<SWIGLU, 128>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
+                                          dev_error, stream);
+        case TILE_256:
+            return launch_tc<SWIGLU, 256>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
+                                          dev_error, stream);
+        default:
+            return launch_tc256<SWIGLU>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,
+                                        stream);
+    }
 }
 
 extern "C" moe_status moe_grouped_gemm_gate_up(const uint16_t *x_perm, const int32_t *offsets,

@@ -6,7 +6,7 @@
 // operands in bf16, so each weight tile is widened in shared memory:
 //
 //   warp 0      TMA producer of the activation tiles (bf16, 128-byte swizzle)
-//   warp 6      TMA producer of the raw int8 weight tiles (own 4-deep ring)
+//   warp 6      TMA producer of the raw int8 weight tiles (own 6-deep ring)
 //   warps 7-14  converters: int8 -> bf16 (exact: |q| <= 127 has 8 significant
 //               bits) into the 128-byte-swizzled K-major layout the MMA reads
 //   warp 1      TMEM allocator + MMA issuer (M = 128 tokens, N = 256 weights)
@@ -20,8 +20,8 @@
 namespace moe {
 
 constexpr int W8_BN = 256;
-constexpr int W8_STAGES = 3;        // activation + converted weight stages
-constexpr int W8_RAW = 4;           // raw int8 weight stages
+constexpr int W8_STAGES = 2;        // activation + converted weight stages
+constexpr int W8_RAW = 6;           // raw int8 weight stages (the HBM stream)
 constexpr int W8_CONV_THREADS = 256;
 constexpr int W8_THREADS = 7 * 32 + W8_CONV_THREADS;
 

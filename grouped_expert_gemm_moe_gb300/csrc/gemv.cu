@@ -24,7 +24,6 @@
 namespace moe {
 
 constexpr int GEMV_THREADS = 256;
-constexpr int GEMV_NR = 4;            // activation rows per pass
 
 // Active (non-empty) groups, compacted by warp 0; validates the offsets.
 struct ActiveGroups {

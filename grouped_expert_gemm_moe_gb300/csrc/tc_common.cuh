@@ -40,12 +40,12 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_tile, const 
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // The per-expert tile table, built by one warp at kernel start from the
-// offsets table: group g owns n_tiles * ceil(rows_g / 128) tiles starting at
+// offsets table: group g owns n_tiles * ceil(rows_g / rows_per_tile) tiles starting at
 // s_tile[g]; s_off mirrors the offsets.  Offsets that are negative, not
 // monotone or beyond M make the whole launch a no-op with a device-check fault.
 __device__ __forceinline__ void build_tile_table(const int32_t *offsets, int G, int M, int n_tiles,
                                                  int *s_off, int *s_tile, int *s_total,
-                                                 int32_t *dev_error) {
+                                                 int32_t *dev_error, int rows_per_tile = TC_BM) {
     const int lane = lane_id();
     int carry = 0;
     bool bad = false;
@@ -55,7 +55,7 @@ __device__ __forceinline__ void build_tile_table(const int32_t *offsets, int G, 
         if (g < G) {
             const int o0 = offsets[g], o1 = offsets[g + 1];
             if (o0 < 0 || o1 < o0 || o1 > M) bad = true;
-            else tiles = ((o1 - o0 + TC_BM - 1) / TC_BM) * n_tiles;
+            else tiles = ((o1 - o0 + rows_per_tile - 1) / rows_per_tile) * n_tiles;
             s_off[g] = o0;
             if (g == G - 1) s_off[G] = o1;
         }

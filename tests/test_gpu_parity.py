@@ -335,10 +335,11 @@ def test_fused_route_permute_limits_and_nan(B, L):
                             torch.empty((1200, 256), dtype=torch.bfloat16, device=DEV))
 
 
-@pytest.mark.parametrize("bn", ["128", "256"])
-def test_gemm_tile_widths_agree(B, L, bn, monkeypatch):
-    """Both tile widths of the tcgen05 GEMM give results within tolerance of
-    the oracle on a DeepSeek-shaped batch (the width is chosen per call)."""
+@pytest.mark.parametrize("tile", ["128", "256", "prefill"])
+def test_gemm_tile_shapes_agree(B, L, tile):
+    """Every tile shape of the tcgen05 GEMM (128 x 128, 128 x 256, 256-row
+    prefill blocks; normally chosen per call from the rows per group) gives
+    results within tolerance of the oracle on a DeepSeek-shaped batch."""
     import subprocess, sys, os
     code = (
         "import sys; sys.path.insert(0, %r)\n"
@@ -356,7 +357,7 @@ def test_gemm_tile_widths_agree(B, L, bn, monkeypatch):
         "print(assert_close(to_np(out)[tok], y, 'bn'))\n"
     ) % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
          os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, MOE_GEMM_BN=bn)
+    env = dict(os.environ, MOE_GEMM_TILE=tile)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
