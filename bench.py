@@ -394,6 +394,75 @@ def e2e_measure(layer, shape, T, inp, K, W, flush):
     return ms, h2d, d2h, out_host.clone()
 
 
+def other_rows(dev, K, W, flush, peaks):
+    """The int8 weight-only layer (OLMoE shapes, T=64, uniform routing) and
+    the 16-layer OLMoE-shaped stack (skewed routing, T=64 and T=2048), each
+    captured in one CUDA graph and timed like the main workload: W warm-up
+    steps, then K (capped for the long stack steps) timed steps with L2
+    flushed before each.  Rooflines: weight bytes of the served groups at
+    HBM bandwidth vs FLOPs at the bf16 peak (sustained for the stack, whose
+    steps run for milliseconds), per layer, summed over the stack."""
+    import torch
+
+    from grouped_expert_gemm_moe_gb300 import binding as B
+    from grouped_expert_gemm_moe_gb300 import workloads as WL
+    from grouped_expert_gemm_moe_gb300.layer import MoELayer, MoEStack
+    rows = {}
+    bw = peaks["hbm_gbs"] * 1e9
+
+    sh = WL.OLMOE_W8
+    T = 64
+    inp = WL.make_layer(sh, T, "uniform", seed=0, device=dev)
+    q_gu, s_gu = B.moe_quantize_w8(inp.w_gu)
+    q_down, s_down = B.moe_quantize_w8(inp.w_down)
+    layer = MoELayer(sh.H, sh.E, sh.k, sh.I, 0, False, q_gu=q_gu.to(dev), s_gu=s_gu.to(dev),
+                     q_down=q_down.to(dev), s_down=s_down.to(dev), device=dev)
+    kind = layer.choose_ffn(T)
+    cap = layer.capture(inp.x, inp.logits, ffn=kind)
+    ms = statistics.fmean(time_graph(cap, K, W, flush))
+    layer.check()
+    ng = touched_groups(layer, layer.buffers(T))
+    H, I = sh.H, sh.I
+    bytes_ = ng * (3 * H * I + (2 * I + H) * 4) + 2 * T * H * 2
+    t_roof = max(bytes_ / bw, 6.0 * H * I * T * sh.k / (peaks["bf16_tflops"] * 1e12)) * 1e6
+    rows["int8_weight_only_t64"] = {
+        "us_per_layer": round(ms * 1e3, 2), "tokens_per_s": round(T / (ms / 1e3), 1),
+        "ffn": kind, "groups": ng, "algorithmic_bytes": bytes_, "bound": "hbm",
+        "t_roof_us": round(t_roof, 2), "roofline_frac": round(t_roof / (ms * 1e3), 4)}
+    del layer, cap, inp, q_gu, q_down
+    torch.cuda.empty_cache()
+
+    sh = WL.OLMOE_STACK
+    for T, K2 in ((64, min(K, 200)), (2048, min(K, 20))):
+        K2 = max(K2, 3)
+        x0, layers_w, bias = WL.make_stack(sh, T, "skew4", seed=0, device=dev)
+        layers = [MoELayer(sh.H, sh.E, sh.k, sh.I, 0, False, w_gu=wg, w_down=wd, device=dev)
+                  for (_, wg, wd) in layers_w]
+        stack = MoEStack(layers, [wr for (wr, _, _) in layers_w], bias)
+        cap = stack.capture(x0)
+        ms = statistics.fmean(time_graph(cap, K2, W, flush))
+        for ly in layers:
+            ly.check()
+        H, I, E, k = sh.H, sh.I, sh.E, sh.k
+        t_roof = 0.0
+        groups = []
+        for ly in layers:
+            ng = touched_groups(ly, ly.buffers(T))
+            groups.append(ng)
+            b_l = ng * 3 * H * I * 2 + 3 * T * H * 2 + E * H * 2
+            f_l = 6.0 * H * I * T * k + 2.0 * T * H * E
+            t_roof += max(b_l / bw, f_l / (peaks["bf16_tflops_sustained"] * 1e12))
+        t_roof *= 1e6
+        rows[f"stack16_t{T}"] = {
+            "us_per_step": round(ms * 1e3, 1), "us_per_layer": round(ms * 1e3 / sh.layers, 2),
+            "tokens_per_s": round(T / (ms / 1e3), 1), "steps": K2,
+            "groups_per_layer": groups, "t_roof_us": round(t_roof, 1),
+            "roofline_frac": round(t_roof / (ms * 1e3), 4)}
+        del stack, layers, layers_w, cap
+        torch.cuda.empty_cache()
+    return rows
+
+
 # ------------------------------------------------------------ oracle legs
 
 def oracle_sample(inp, tokens):
@@ -496,6 +565,10 @@ def run_ours(args):
                           "gate_up_frac": m2["kroof"]["frac"], "groups": m2["n_groups"]}
     layer.check()
 
+    rows = None
+    if world == 1 and not args.no_rows:
+        rows = other_rows(dev, args.steps, args.warmup, flush, peaks)
+
     e2e_ms, h2d, d2h, out_e2e = e2e_measure(layer, shape, T, inp, args.steps, args.warmup, flush)
     layer.check()
     e2e_sec = reduce_max(e2e_ms * args.steps / 1e3, world, dev)
@@ -527,6 +600,7 @@ def run_ours(args):
                                "peak_source": peaks["source"]},
             "roofline": m["kroof"],
             "per_T": per_T,
+            "other_rows": rows,
             "e2e": {"value": round(aggregate_value(T * args.steps, world, e2e_sec), 1),
                     "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": round(e2e_ms * 1e3, 2),
@@ -594,6 +668,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the int8 and 16-layer stack measurements of other_rows")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

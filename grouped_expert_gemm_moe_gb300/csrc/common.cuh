@@ -119,11 +119,13 @@ __device__ __forceinline__ float s8_to_f32(uint32_t word_biased, int byte_idx) {
 __device__ __forceinline__ uint32_t bias_s8x4(uint32_t w) { return w ^ 0x80808080u; }
 
 // ---- loads
-__device__ __forceinline__ uint4 ld_stream(const void *p) {   // read-once data
+// read-once data: no L1 allocation, L2 line marked by `policy` (evict-first
+// for weight streams, so they do not push out what is wanted again)
+__device__ __forceinline__ uint4 ld_stream(const void *p, uint64_t policy) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+                 : "l"(p), "l"(policy));
     return r;
 }
 __device__ __forceinline__ uint4 ld_nc(const void *p) {       // read-only, cached
@@ -195,6 +197,11 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // 2-D tiled TMA load global -> shared, completion counted on `bar` in bytes.

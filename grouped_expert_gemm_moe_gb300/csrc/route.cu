@@ -27,48 +27,71 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
     }
 }
 
-// logits[t,e] = sum_c x[t,c] * w_r[e,c] (+ bias[e]).  A block computes a
-// 16-token x 64-expert tile; x and w_r chunks of 64 columns are staged in
-// shared memory as fp32; every output is summed over c in ascending order.
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t *__restrict__ x,
-                                                            const uint16_t *__restrict__ w_r,
-                                                            const float *__restrict__ bias,
-                                                            int T, int H, int E,
-                                                            float *__restrict__ logits) {
-    __shared__ float xs[16][65];
-    __shared__ float ws[64][65];
+// logits[t,e] = sum_c x[t,c] * w_r[e,c] (+ bias[e]).  A block computes TOK
+// tokens x 64 experts; its 8 warps split the hidden dimension into 8
+// contiguous ranges of 16-byte chunks, and lane l of a warp owns experts
+// e0+l and e0+l+32 for all TOK tokens.  Per chunk a lane reads its two
+// w_r chunks and the TOK x chunks (the same address across the warp, one
+// broadcast each).  Each warp's partial sums (columns ascending) are then
+// added in warp order 0..7 through shared memory, so every logit has one
+// fixed summation order.
+constexpr int RL_WARPS = 8;
+
+template <int TOK>
+__global__ void __launch_bounds__(RL_WARPS * 32) router_logits_kernel(
+    const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_r,
+    const float *__restrict__ bias, int T, int H, int E, float *__restrict__ logits) {
+    __shared__ float part[RL_WARPS][TOK][64];
     pdl_wait();
     pdl_trigger();
-    const int t0 = blockIdx.x * 16, e0 = blockIdx.y * 64;
-    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < H; c0 += 64) {
-        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-            const int r = i / 64, c = i % 64;
-            const int t = t0 + r, cc = c0 + c;
-            xs[r][c] = (t < T && cc < H) ? bf_lo(x[static_cast<size_t>(t) * H + cc]) : 0.f;
-        }
-        for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-            const int r = i / 64, c = i % 64;
-            const int e = e0 + r, cc = c0 + c;
-            ws[r][c] = (e < E && cc < H) ? bf_lo(w_r[static_cast<size_t>(e) * H + cc]) : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int c = 0; c < 64; ++c) {
-            const float xv = xs[ty][c];
+    const int lane = lane_id(), warp = threadIdx.x >> 5;
+    const int t0 = blockIdx.x * TOK, e0 = blockIdx.y * 64;
+    const int chunks = H / 8;
+    const int c_begin = warp * chunks / RL_WARPS, c_end = (warp + 1) * chunks / RL_WARPS;
+    const int ea = e0 + lane, eb = e0 + lane + 32;
+    const bool has_a = ea < E, has_b = eb < E;
+    const uint16_t *wa = w_r + static_cast<int64_t>(has_a ? ea : 0) * H;
+    const uint16_t *wb = w_r + static_cast<int64_t>(has_b ? eb : 0) * H;
+    const uint16_t *xr[TOK];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = fmaf(xv, ws[tx + 16 * q][c], acc[q]);
+    for (int i = 0; i < TOK; ++i)
+        xr[i] = x + static_cast<int64_t>(t0 + i < T ? t0 + i : 0) * H;
+    float acc[TOK][2];
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) acc[i][0] = acc[i][1] = 0.f;
+#pragma unroll 4
+    for (int c = c_begin; c < c_end; ++c) {
+        const uint4 va = ld_nc(wa + c * 8), vb = ld_nc(wb + c * 8);
+        uint4 vx[TOK];
+#pragma unroll
+        for (int i = 0; i < TOK; ++i) vx[i] = ld_nc(xr[i] + c * 8);
+        const uint32_t pa[4] = {va.x, va.y, va.z, va.w}, pb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+        for (int i = 0; i < TOK; ++i) {
+            const uint32_t px[4] = {vx[i].x, vx[i].y, vx[i].z, vx[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x0 = bf_lo(px[q]), x1 = bf_hi(px[q]);
+                acc[i][0] = fmaf(x0, bf_lo(pa[q]), acc[i][0]);
+                acc[i][0] = fmaf(x1, bf_hi(pa[q]), acc[i][0]);
+                acc[i][1] = fmaf(x0, bf_lo(pb[q]), acc[i][1]);
+                acc[i][1] = fmaf(x1, bf_hi(pb[q]), acc[i][1]);
+            }
         }
-        __syncthreads();
     }
-    const int t = t0 + ty;
-    if (t < T) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = e0 + tx + 16 * q;
-            if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[q] + (bias ? bias[e] : 0.f);
-        }
+    for (int i = 0; i < TOK; ++i) {
+        part[warp][i][lane] = acc[i][0];
+        part[warp][i][lane + 32] = acc[i][1];
+    }
+    __syncthreads();
+    for (int o = threadIdx.x; o < TOK * 64; o += blockDim.x) {
+        const int i = o / 64, e = e0 + o % 64, t = t0 + i;
+        if (t >= T || e >= E) continue;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < RL_WARPS; ++w) v += part[w][i][o % 64];
+        logits[static_cast<int64_t>(t) * E + e] = v + (bias ? bias[e] : 0.f);
     }
 }
 
@@ -105,7 +128,17 @@ extern "C" moe_status moe_router_logits(const uint16_t *x, const uint16_t *w_r, 
     if (!x || !w_r || !logits || T < 1 || H < 1 || E < 1) return MOE_ERR_INVALID_ARG;
     if (static_cast<int64_t>(T) * H >= (1ll << 31) || static_cast<int64_t>(E) * H >= (1ll << 31))
         return MOE_ERR_UNSUPPORTED;
-    dim3 grid((T + 15) / 16, (E + 63) / 64);
-    launch(router_logits_kernel, grid, 256, 0, stream, x, w_r, bias, T, H, E, logits);
+    if (H % 8 != 0) return MOE_ERR_ALIGNMENT;
+    if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_ALIGNMENT;
+    // few tokens per block for small batches (more blocks), 8 for large ones
+    if (T <= 512) {
+        dim3 grid((T + 1) / 2, (E + 63) / 64);
+        launch(router_logits_kernel<2>, grid, RL_WARPS * 32, 0, stream, x, w_r, bias, T, H, E,
+               logits);
+    } else {
+        dim3 grid((T + 7) / 8, (E + 63) / 64);
+        launch(router_logits_kernel<8>, grid, RL_WARPS * 32, 0, stream, x, w_r, bias, T, H, E,
+               logits);
+    }
     return launch_status();
 }

@@ -16,7 +16,7 @@ from . import binding as B
 
 # Mean permuted rows per expert group at or below which the grouped GEMV is
 # used instead of the tensor-core grouped GEMM.
-GEMV_MAX_ROWS_PER_GROUP = 2.0
+GEMV_MAX_ROWS_PER_GROUP = 0.25
 
 
 @dataclass
@@ -214,3 +214,26 @@ class MoEStack:
             layer.forward(cur, L, out=nxt, residual=cur, ffn=ffn, stream=stream)
             cur = nxt
         return cur
+
+    def capture(self, x: torch.Tensor, ffn="auto") -> "CapturedStack":
+        """Record one pass over all blocks (router logits included) into a
+        CUDA graph; replay() reruns it on whatever the fixed buffer x holds."""
+        return CapturedStack(self, x, ffn)
+
+
+class CapturedStack:
+    """A whole-stack forward pass recorded into one CUDA graph."""
+
+    def __init__(self, stack: MoEStack, x: torch.Tensor, ffn):
+        self.stack, self.x = stack, x
+        stack.forward(x, ffn=ffn)               # eager pass: buffers and kernel attributes
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            self.out = stack.forward(x, ffn=ffn)
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
+

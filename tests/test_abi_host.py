@@ -127,6 +127,15 @@ def test_ffn_argument_checks(lib):
              None) == 3
 
 
+def test_router_logits_argument_checks(lib):
+    f = lib.moe_router_logits
+    f.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
+    assert f(None, GOOD, None, 4, 64, 8, GOOD, None) == 1
+    assert f(GOOD, GOOD, None, 0, 64, 8, GOOD, None) == 1
+    assert f(GOOD, GOOD, None, 4, 60, 8, GOOD, None) == 3          # H not a multiple of 8
+    assert f(ODD, GOOD, None, 4, 64, 8, GOOD, None) == 3
+
+
 def test_combine_argument_checks(lib):
     f = lib.moe_combine
     f.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]

@@ -160,3 +160,23 @@ def test_stack_teacher_forced(mods, T, ffn):
           f"{np.round(max_load, 2).tolist()}")
     if T == 2048:
         assert 3.5 <= max_load[0] <= 4.5
+
+
+def test_stack_graph_replay_matches_eager(mods):
+    """The whole stack captured in one CUDA graph gives the eager bytes, and
+    a replay after new input is written into the captured buffer follows it."""
+    B, L = mods
+    sh = W.OLMOE_STACK
+    x0, layers_w, bias = W.make_stack(sh, 64, "skew4", seed=1, device=DEV)
+    layers = [L.MoELayer(sh.H, sh.E, sh.k, sh.I, 0, False, w_gu=wg, w_down=wd, device=DEV)
+              for (_, wg, wd) in layers_w]
+    stack = L.MoEStack(layers, [wr for (wr, _, _) in layers_w], bias)
+    cap = stack.capture(x0)
+    for trial in range(2):
+        got = cap.replay().clone()
+        want = stack.forward(x0).clone()
+        for layer in layers:
+            layer.check()
+        assert torch.equal(got, want), f"trial {trial}"
+        g = torch.Generator(device=DEV).manual_seed(11 + trial)
+        x0.copy_(torch.randn(x0.shape, generator=g, device=DEV).to(torch.bfloat16))
