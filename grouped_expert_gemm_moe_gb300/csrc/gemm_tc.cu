@@ -299,38 +299,58 @@ template <bool SWIGLU>
 moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, int G, int M,
                         int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
                         cudaStream_t stream);
-}  // namespace moe
 
-// Tile shape per call, from the mean rows per group (M / G):
+// Tile shape per call, from the mean rows per group (M / G), chosen from
+// GB300 measurements of the OLMoE-shaped layer (bf16 and int8 weights):
+//   <= 8 rows  : 128 x 128 tiles (a decode batch: every weight tile is read
+//                once either way, and this kernel's hand-offs are cheapest);
+//   <= 20 / 48 rows: weight-row tiles (gemm_tc_dec.cu) with token blocks of
+//                32 / 64 rows: the MMA's 128 rows are weight rows, so no
+//                tensor-core time goes to empty token rows (7-8 % faster than
+//                128 x 128 at 16 and 32 rows per group);
 //   <= 64 rows : 128 x 128 tiles (twice the tiles of 128 x 256, which evens
 //                out the last wave when the groups are small);
 //   <= 512 rows: 128 x 256 tiles;
 //   more       : 256-row token blocks x 256 weight rows (gemm_tc256.cu), which
 //                need a third fewer operand bytes per FLOP and win once most
-//                groups fill several blocks (measured on GB300: 0.73 of bf16
-//                peak at 1024 rows per group against 0.65 for 128 x 256).
-// MOE_GEMM_TILE=128|256|prefill in the environment overrides the choice.
-enum { TILE_128 = 0, TILE_256 = 1, TILE_PREFILL = 2 };
-static int pick_tile(int M, int G) {
+//                groups fill several blocks (0.73 of bf16 peak at 1024 rows
+//                per group against 0.65 for 128 x 256).
+// MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill in the environment
+// overrides the choice.
+int pick_tile(int M, int G) {
     static const int forced = [] {
         const char *v = getenv("MOE_GEMM_TILE");
         if (!v) return -1;
+        if (!strcmp(v, "dec16")) return static_cast<int>(TILE_DEC16);
+        if (!strcmp(v, "dec32")) return static_cast<int>(TILE_DEC32);
+        if (!strcmp(v, "dec64")) return static_cast<int>(TILE_DEC64);
         if (!strcmp(v, "128")) return static_cast<int>(TILE_128);
         if (!strcmp(v, "256")) return static_cast<int>(TILE_256);
         if (!strcmp(v, "prefill")) return static_cast<int>(TILE_PREFILL);
         return -1;
     }();
     if (forced >= 0) return forced;
-    if (static_cast<int64_t>(M) <= 64ll * G) return TILE_128;
-    if (static_cast<int64_t>(M) <= 512ll * G) return TILE_256;
+    const int64_t m = M, g = G;
+    if (m <= 8 * g) return TILE_128;
+    if (m <= 20 * g) return TILE_DEC32;
+    if (m <= 48 * g) return TILE_DEC64;
+    if (m <= 64 * g) return TILE_128;
+    if (m <= 512 * g) return TILE_256;
     return TILE_PREFILL;
 }
+}  // namespace moe
 
 template <bool SWIGLU>
 static moe_status launch_tc_bn(const void *act, const void *w, const int32_t *offsets, int G,
                                int M, int K, int R, int NOUT, int UP_OFF, uint16_t *out,
                                int32_t *dev_error, cudaStream_t stream) {
-    switch (pick_tile(M, G)) {
+    const int tile = pick_tile(M, G);
+    switch (tile) {
+        case TILE_DEC16:
+        case TILE_DEC32:
+        case TILE_DEC64:
+            return launch_dec<SWIGLU, false>(dec_tn(tile), act, w, nullptr, offsets, G, M, K, R,
+                                             NOUT, UP_OFF, out, dev_error, stream);
         case TILE_128:
             return launch_tc<SWIGLU, 128>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
                                           dev_error, stream);

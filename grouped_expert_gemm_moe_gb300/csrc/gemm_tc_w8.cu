@@ -6,10 +6,14 @@
 // operands in bf16, so each weight tile is widened in shared memory:
 //
 //   warp 0      TMA producer of the activation tiles (bf16, 128-byte swizzle)
-//   warp 6      TMA producer of the raw int8 weight tiles (own 6-deep ring)
-//   warps 7-14  converters: int8 -> bf16 (exact: |q| <= 127 has 8 significant
-//               bits) into the 128-byte-swizzled K-major layout the MMA reads
+//   warp 6      TMA producer of the raw int8 weight tiles (own 4-deep ring)
+//   warps 7-14  converters, four groups taking turns by k-step: int8 -> bf16
+//               (exact: |q| <= 127 has 8 significant bits) into the
+//               128-byte-swizzled K-major layout the MMA reads
 //   warp 1      TMEM allocator + MMA issuer (M = 128 tokens, N = 256 weights)
+//
+// Decode-sized groups go to the weight-row tiles of gemm_tc_dec.cu instead
+// (same widening, with the MMA's 128 rows spent on weight rows).
 //   warps 2-5   epilogue: accumulator * per-row scale (= sum x*q*scale, the
 //               dequantised product), then SwiGLU or a plain bf16 store.
 //
@@ -20,8 +24,8 @@
 namespace moe {
 
 constexpr int W8_BN = 256;
-constexpr int W8_STAGES = 2;        // activation + converted weight stages
-constexpr int W8_RAW = 6;           // raw int8 weight stages (the HBM stream)
+constexpr int W8_STAGES = 3;        // activation + converted weight stages
+constexpr int W8_RAW = 4;           // raw int8 weight stages (the HBM stream)
 constexpr int W8_CONV_THREADS = 256;
 constexpr int W8_THREADS = 7 * 32 + W8_CONV_THREADS;
 
@@ -37,26 +41,6 @@ struct W8Cfg {
                2 * static_cast<size_t>(G + 1) * sizeof(int);
     }
 };
-
-// 16 int8 -> 16 bf16 (two 16-byte chunks), exactly.
-__device__ __forceinline__ void widen16(const uint4 v, uint4 &lo, uint4 &hi) {
-    const uint32_t w[4] = {bias_s8x4(v.x), bias_s8x4(v.y), bias_s8x4(v.z), bias_s8x4(v.w)};
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float f0 = s8_to_f32(w[i], 0), f1 = s8_to_f32(w[i], 1);
-        const float f2 = s8_to_f32(w[i], 2), f3 = s8_to_f32(w[i], 3);
-        // the upper half of an fp32 holding a small integer is its exact bf16
-        o[2 * i] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-        o[2 * i + 1] = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
-    }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // SWIGLU: out = h [M, NOUT=I], int8 weights [G*2I, K=H], scales [G*2I].
 // PLAIN : out = y [M, NOUT=H], int8 weights [G*H,  K=I], scales [G*H].
@@ -97,12 +81,12 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&a_full[s], 1);
-            mbar_init(&b_full[s], W8_CONV_THREADS);
+            mbar_init(&b_full[s], W8_GROUP_THREADS);
             mbar_init(&ab_empty[s], 1);
         }
         for (int r = 0; r < RS; ++r) {
             mbar_init(&q_full[r], 1);
-            mbar_init(&q_empty[r], W8_CONV_THREADS);
+            mbar_init(&q_empty[r], W8_GROUP_THREADS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
@@ -193,35 +177,23 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
     } else if (warp >= 7) {
         // ------------------------------------------- converters int8 -> bf16
         const int ct = threadIdx.x - 7 * 32;
-        int s = 0, r = 0;
-        uint32_t sph = 0, rph = 0;
+        const int grp = ct / W8_GROUP_THREADS, gt = ct % W8_GROUP_THREADS;
+        int seq = 0;                                   // this CTA's k-step counter
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = 0; kb < KB; ++kb, ++seq) {
+                if (seq % W8_GROUPS != grp) continue;
+                const int s = seq % S, r = seq % RS;
+                const uint32_t sph = (seq / S) & 1, rph = (seq / RS) & 1;
                 if (!mbar_wait(&q_full[r], rph, dev_error) ||
                     !mbar_wait(&ab_empty[s], sph ^ 1u, dev_error)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *q = sQ + r * C::RAW_BYTES;
-                uint8_t *b = sB + s * C::B_BYTES;
-#pragma unroll
-                for (int p = 0; p < (BN * 4) / W8_CONV_THREADS; ++p) {
-                    const int chunk = ct + p * W8_CONV_THREADS;     // 16 int8 each
-                    const int row = chunk >> 2, part = chunk & 3;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(q + row * TC_BK + part * 16);
-                    uint4 lo, hi;
-                    widen16(v, lo, hi);
-                    uint8_t *brow = b + row * 128;
-                    const int sw = row & 7;
-                    *reinterpret_cast<uint4 *>(brow + (((2 * part) ^ sw) << 4)) = lo;
-                    *reinterpret_cast<uint4 *>(brow + (((2 * part + 1) ^ sw) << 4)) = hi;
-                }
+                widen_stage<BN>(sQ + r * C::RAW_BYTES, sB + s * C::B_BYTES, gt);
                 fence_proxy_async_smem();     // generic-proxy writes -> visible to the MMA
                 mbar_arrive(&b_full[s]);
                 mbar_arrive(&q_empty[r]);
-                if (++s == S) { s = 0; sph ^= 1u; }
-                if (++r == RS) { r = 0; rph ^= 1u; }
             }
         }
     } else if (warp == 1) {
@@ -355,6 +327,10 @@ template <bool SWIGLU>
 static moe_status launch_tc_w8(const void *act, const int8_t *q, const float *scales,
                                const int32_t *offsets, int G, int M, int K, int R, int NOUT,
                                int UP_OFF, uint16_t *out, int32_t *dev_error, cudaStream_t stream) {
+    const int tile = pick_tile(M, G);
+    if (tile == TILE_DEC16 || tile == TILE_DEC32 || tile == TILE_DEC64)
+        return launch_dec<SWIGLU, true>(dec_tn(tile), act, q, scales, offsets, G, M, K, R, NOUT,
+                                        UP_OFF, out, dev_error, stream);
     CUtensorMap tm_act, tm_q;
     CUtensorMap tm_act128;
     if (!encode_bf16_2d(&tm_act, act, K, M, TC_ABOX)) return MOE_ERR_CUDA;

@@ -17,8 +17,10 @@ struct TileInfo {
     int g, nt, m0, nrows;
 };
 
-// s_tile[g] = first linear tile of group g (s_tile[G] = total).
-__device__ __forceinline__ TileInfo decode_tile(int t, const int *s_tile, const int *s_off, int G) {
+// s_tile[g] = first linear tile of group g (s_tile[G] = total); a group's
+// rows are cut into blocks of rows_per_tile, the block index running fastest.
+__device__ __forceinline__ TileInfo decode_tile(int t, const int *s_tile, const int *s_off, int G,
+                                                int rows_per_tile = TC_BM) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -29,15 +31,72 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_tile, const 
     ti.g = lo;
     const int u = t - s_tile[lo];
     const int rows = s_off[lo + 1] - s_off[lo];
-    const int mt_count = (rows + TC_BM - 1) / TC_BM;
+    const int mt_count = (rows + rows_per_tile - 1) / rows_per_tile;
     ti.nt = u / mt_count;
     const int mt = u - ti.nt * mt_count;
-    ti.m0 = s_off[lo] + mt * TC_BM;
-    ti.nrows = min(TC_BM, rows - mt * TC_BM);
+    ti.m0 = s_off[lo] + mt * rows_per_tile;
+    ti.nrows = min(rows_per_tile, rows - mt * rows_per_tile);
     return ti;
 }
 
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// Two int8 in bits 0-7 and 16-23 of `spread` -> bf16x2, exactly.  With b
+// the byte and m = b & 0x7F, the bf16 bit pattern 0x4300 | m is 128 + m and
+// 0x4300 | (b & 0x80) is 128 (b >= 0) or 256 (b < 0), so their difference is
+// the two's-complement value of b; it is an integer below 256 in magnitude,
+// which bf16 holds exactly, so the rounded subtraction is exact.
+__device__ __forceinline__ uint32_t s8x2_to_bf16x2(uint32_t spread) {
+    const uint32_t val = (spread & 0x007F007Fu) | 0x43004300u;
+    const uint32_t sub = (spread & 0x00800080u) | 0x43004300u;
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(val), "r"(sub));
+    return r;
+}
+
+// 16 int8 -> 16 bf16 (two 16-byte chunks), exactly, in K order.
+__device__ __forceinline__ void widen16(const uint4 v, uint4 &lo, uint4 &hi) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = s8x2_to_bf16x2(__byte_perm(w[i], 0u, 0x4140));       // bytes 0, 1
+        o[2 * i + 1] = s8x2_to_bf16x2(__byte_perm(w[i], 0u, 0x4342));   // bytes 2, 3
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The int8 converters work in W8_GROUPS independent groups of
+// W8_GROUP_THREADS threads; group c widens the k-steps c, c + W8_GROUPS, ...
+// of the CTA's sequence, so that several stages are converted at once and
+// the conversion latency (shared-memory round trips, the proxy fence, the
+// barrier hand-off) overlaps instead of adding up stage after stage.
+constexpr int W8_GROUPS = 4;
+constexpr int W8_GROUP_THREADS = 64;
+
+// One raw int8 stage (ROWS rows x 64 bytes, row-major, as TMA left it) ->
+// bf16 in the 128-byte-swizzled K-major layout (16-byte unit u of row r at
+// unit u ^ (r & 7)).  gt: this thread's index in its converter group.
+template <int ROWS>
+__device__ __forceinline__ void widen_stage(const uint8_t *q, uint8_t *a, int gt) {
+#pragma unroll 4
+    for (int p = 0; p < (ROWS * 4) / W8_GROUP_THREADS; ++p) {
+        const int chunk = gt + p * W8_GROUP_THREADS;              // 16 int8 each
+        const int row = chunk >> 2, part = chunk & 3;
+        const uint4 v = *reinterpret_cast<const uint4 *>(q + row * TC_BK + part * 16);
+        uint4 lo, hi;
+        widen16(v, lo, hi);
+        uint8_t *arow = a + row * 128;
+        const int sw = row & 7;
+        *reinterpret_cast<uint4 *>(arow + (((2 * part) ^ sw) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(arow + (((2 * part + 1) ^ sw) << 4)) = hi;
+    }
+}
 
 // The per-expert tile table, built by one warp at kernel start from the
 // offsets table: group g owns n_tiles * ceil(rows_g / rows_per_tile) tiles starting at
@@ -128,6 +187,17 @@ inline bool raise_smem_limit(Kernel kernel, int *done_per_device) {
     }
     return true;
 }
+
+// Tile shapes of the grouped GEMMs (gemm_tc.cu picks one per call).
+enum { TILE_DEC16 = 0, TILE_DEC32, TILE_DEC64, TILE_128, TILE_256, TILE_PREFILL };
+int pick_tile(int M, int G);
+inline int dec_tn(int tile) { return tile == TILE_DEC16 ? 16 : tile == TILE_DEC32 ? 32 : 64; }
+
+// Weight-row tiles for decode-sized groups (gemm_tc_dec.cu); scales: int8 only.
+template <bool SWIGLU, bool W8>
+moe_status launch_dec(int tn, const void *tok, const void *w, const float *scales,
+                      const int32_t *offsets, int G, int M, int K, int R, int NOUT, int UP_OFF,
+                      uint16_t *out, int32_t *dev_error, cudaStream_t stream);
 
 moe_status check_ffn_args(const void *x_perm, const int32_t *offsets, int G, int M, int H, int I,
                           const void *w_gu, const void *w_down, const void *y_perm,

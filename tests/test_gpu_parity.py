@@ -131,7 +131,12 @@ def _ffn_rows_oracle(xp_bits, off, w_gu_bits, w_down_bits, H, I):
 @pytest.mark.parametrize("ffn", ["gemm", "gemv"])
 @pytest.mark.parametrize("H,I,E,S,k,T", [(136, 200, 5, 1, 2, 300),     # K and N tails
                                           (256, 512, 4, 0, 1, 1000),   # several m-tiles + tail
-                                          (512, 384, 16, 2, 4, 97)])
+                                          (512, 384, 16, 2, 4, 97),
+                                          # decode-sized groups (weight-row tiles with
+                                          # 16/32/64-token blocks), ragged K, N and blocks
+                                          (136, 200, 5, 1, 2, 12),
+                                          (136, 200, 5, 1, 2, 40),
+                                          (136, 200, 5, 1, 2, 90)])
 def test_grouped_ffn_rows_vs_oracle(B, L, ffn, H, I, E, S, k, T):
     """The grouped FFN alone: every permuted row against the oracle's expert
     FFN, on shapes whose tiles have ragged M, N and K tails."""
@@ -335,11 +340,13 @@ def test_fused_route_permute_limits_and_nan(B, L):
                             torch.empty((1200, 256), dtype=torch.bfloat16, device=DEV))
 
 
-@pytest.mark.parametrize("tile", ["128", "256", "prefill"])
+@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "128", "256", "prefill"])
 def test_gemm_tile_shapes_agree(B, L, tile):
-    """Every tile shape of the tcgen05 GEMM (128 x 128, 128 x 256, 256-row
-    prefill blocks; normally chosen per call from the rows per group) gives
-    results within tolerance of the oracle on a DeepSeek-shaped batch."""
+    """Every tile shape of the tcgen05 GEMM (weight-row tiles with 16/32/64-
+    token blocks, 128 x 128, 128 x 256, 256-row prefill blocks; normally
+    chosen per call from the rows per group) gives results within tolerance
+    of the oracle on a DeepSeek-shaped batch (zipf routing: group sizes from
+    a few rows to the 512-row shared experts)."""
     import subprocess, sys, os
     code = (
         "import sys; sys.path.insert(0, %r)\n"

@@ -78,7 +78,9 @@ def test_w8_layer_matches_oracle(mods, T, routing, ffn):
     print(f"w8 {ffn} T={T} {routing}: rel {rel:.2e} max {mx:.2e}")
 
 
-@pytest.mark.parametrize("H,I,E,S,k,T", [(144, 208, 5, 1, 2, 300), (256, 512, 4, 0, 1, 1000)])
+@pytest.mark.parametrize("H,I,E,S,k,T", [(144, 208, 5, 1, 2, 300), (256, 512, 4, 0, 1, 1000),
+                                          (144, 208, 5, 1, 2, 12), (144, 208, 5, 1, 2, 40),
+                                          (144, 208, 5, 1, 2, 90)])
 def test_w8_gemm_rows_vs_oracle(mods, H, I, E, S, k, T):
     """Every permuted row of the int8 tensor-core FFN on ragged tiles."""
     B, L = mods
