@@ -93,10 +93,15 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of every CUDA source: a committed traffic figure is used only
+    while the kernels it was measured on are unchanged."""
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "gemv.cu", "common.cuh"):
-        with open(os.path.join(ROOT, "grouped_expert_gemm_moe_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "grouped_expert_gemm_moe_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -199,11 +199,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // 2-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y, uint64_t policy) {

@@ -67,28 +67,6 @@ __device__ __forceinline__ int load_active_groups(ActiveGroups &ag, const int32_
     return ag.count;
 }
 
-// While the gate/up pass streams its weights, the down weights of the
-// active groups are pulled into L2 alongside when they fit in
-// `budget_bytes`, so the down pass reads them from L2 instead of starting a
-// second HBM stream after a launch gap.  Work is split in 64 KB pieces over
-// every warp of the grid; lane 0 issues the bulk prefetch.
-__device__ __forceinline__ void prefetch_down_l2(const ActiveGroups &ag, int na,
-                                                 const uint8_t *w_down, int64_t group_bytes,
-                                                 int64_t budget_bytes) {
-    if (w_down == nullptr || static_cast<int64_t>(na) * group_bytes > budget_bytes) return;
-    if (lane_id() != 0) return;
-    constexpr int64_t PIECE = 64 << 10;
-    const int64_t per_group = (group_bytes + PIECE - 1) / PIECE;
-    const int64_t wpb = blockDim.x >> 5;
-    const int64_t nw = static_cast<int64_t>(gridDim.x) * wpb;
-    for (int64_t p = blockIdx.x * wpb + (threadIdx.x >> 5); p < na * per_group; p += nw) {
-        const int a = static_cast<int>(p / per_group);
-        const int64_t off = (p % per_group) * PIECE;
-        prefetch_l2_bulk(w_down + ag.group[a] * group_bytes + off,
-                         static_cast<uint32_t>(min(PIECE, group_bytes - off)));
-    }
-}
-
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
@@ -118,14 +96,12 @@ __device__ __forceinline__ void unpack16_s8(const uint4 v, float (&f)[16]) {
 template <int NCH, int NR>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_bf16(
     const uint16_t *__restrict__ x_perm, const int32_t *__restrict__ offsets, int G, int M, int H,
-    int I, const uint16_t *__restrict__ w_gu, uint16_t *__restrict__ h, int32_t *dev_error,
-    const uint8_t *w_down_pf, int64_t pf_group_bytes, int64_t pf_budget) {
+    int I, const uint16_t *__restrict__ w_gu, uint16_t *__restrict__ h, int32_t *dev_error) {
     __shared__ ActiveGroups ag;
     pdl_wait();
     pdl_trigger();
     const int na = load_active_groups(ag, offsets, G, M, dev_error);
     const uint64_t pol = policy_evict_first();
-    prefetch_down_l2(ag, na, w_down_pf, pf_group_bytes, pf_budget);
     const int lane = lane_id(), wpb = blockDim.x >> 5;
     const int chunks = H / 8;
     const int64_t ntasks = static_cast<int64_t>(na) * I;
@@ -270,14 +246,12 @@ template <int NCH, int NR>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_w8(
     const uint16_t *__restrict__ x_perm, const int32_t *__restrict__ offsets, int G, int M, int H,
     int I, const int8_t *__restrict__ q_gu, const float *__restrict__ s_gu,
-    uint16_t *__restrict__ h, int32_t *dev_error, const uint8_t *w_down_pf,
-    int64_t pf_group_bytes, int64_t pf_budget) {
+    uint16_t *__restrict__ h, int32_t *dev_error) {
     __shared__ ActiveGroups ag;
     pdl_wait();
     pdl_trigger();
     const int na = load_active_groups(ag, offsets, G, M, dev_error);
     const uint64_t pol = policy_evict_first();
-    prefetch_down_l2(ag, na, w_down_pf, pf_group_bytes, pf_budget);
     const int lane = lane_id(), wpb = blockDim.x >> 5;
     const int chunks = H / 16;                   // 16 int8 per 16-byte chunk
     const int64_t ntasks = static_cast<int64_t>(na) * I;
@@ -437,10 +411,6 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_w8(
 
 // ------------------------------------------------------------------ host
 
-// Largest down-weight set (bytes) the gate/up pass pulls into L2 for the
-// down pass: half of the 126 MB L2, leaving room for the activations.
-constexpr int64_t DOWN_PREFETCH_BUDGET = int64_t(64) << 20;
-
 static int pick_nch(int chunks) {            // chunks = 16-byte chunks per row
     const int per_lane = (chunks + 31) / 32;
     return per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : 8;
@@ -566,8 +536,7 @@ extern "C" moe_status moe_grouped_gemv_gate_up(const uint16_t *x_perm, const int
                                                cudaStream_t stream) {
     moe_status st = check_phase_args(x_perm, offsets, G, M, H, I, w_gu, h, 8);
     if (st != MOE_OK) return st;
-    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error,
-                       static_cast<const uint8_t *>(nullptr), int64_t(0), int64_t(0));
+    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
     return launch_status();
 }
 
@@ -590,9 +559,7 @@ extern "C" moe_status moe_grouped_gemv(const uint16_t *x_perm, const int32_t *of
                                    workspace_bytes, 8);
     if (st != MOE_OK) return st;
     uint16_t *h = static_cast<uint16_t *>(workspace);
-    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error,
-                       reinterpret_cast<const uint8_t *>(w_down), int64_t(H) * I * 2,
-                       DOWN_PREFETCH_BUDGET);
+    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
     if ((st = launch_status()) != MOE_OK) return st;
     launch_down_bf16(pick_nch(I / 8), pick_nr(M, G), stream, static_cast<const uint16_t *>(h), offsets, G, M, H, I,
                      w_down, y_perm, dev_error);
@@ -611,8 +578,7 @@ extern "C" moe_status moe_grouped_gemv_w8(const uint16_t *x_perm, const int32_t 
     if (!s_gu || !s_down) return MOE_ERR_INVALID_ARG;
     uint16_t *h = static_cast<uint16_t *>(workspace);
     launch_gateup_w8(pick_nch(H / 16), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, q_gu, s_gu, h,
-                     dev_error, reinterpret_cast<const uint8_t *>(q_down), int64_t(H) * I,
-                     DOWN_PREFETCH_BUDGET);
+                     dev_error);
     if ((st = launch_status()) != MOE_OK) return st;
     launch_down_w8(pick_nch(I / 16), pick_nr(M, G), stream, static_cast<const uint16_t *>(h), offsets, G, M, H, I,
                    q_down, s_down, y_perm, dev_error);
@@ -676,9 +642,7 @@ extern "C" moe_status moe_grouped_gemv_noalloc(const uint16_t *x_perm, const int
     if (h == nullptr) return st;
     // Nothing in the scratch has to start at zero: the gate/up pass writes
     // every h row of every non-empty group before the down pass reads it.
-    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error,
-                       reinterpret_cast<const uint8_t *>(w_down), int64_t(H) * I * 2,
-                       DOWN_PREFETCH_BUDGET);
+    launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);
     if ((st = launch_status()) != MOE_OK) return st;
     launch_down_bf16(pick_nch(I / 8), pick_nr(M, G), stream, static_cast<const uint16_t *>(h), offsets, G, M, H,
                      I, w_down, y_perm, dev_error);
