@@ -81,8 +81,22 @@ __device__ __forceinline__ void copy_row(const void *__restrict__ x, int64_t t, 
                                 pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
         }
     } else {
+        // up to 8 chunks per lane loaded before any is stored, so a warp
+        // keeps a whole 4 KB row in flight
         const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + t * H);
-        for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+        for (int c0 = 0; c0 < chunks; c0 += 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < chunks) v[u] = __ldg(src + c);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < chunks) dst[c] = v[u];
+            }
+        }
     }
 }
 

@@ -10,6 +10,7 @@ from .oracle import (  # noqa: F401
     load,
     route,
     permute,
+    permute_capped,
     expert_hidden,
     expert_down,
     moe_layer,

@@ -24,6 +24,13 @@
  *            ("switchyard" page, "One launch for all experts": grouped GEMM
  *             with SwiGLU; "dispatch" README, Stack: shared + routed
  *             experts.)
+ *   capacity: the dropping variant.  Routed expert e serves at most C of
+ *            its slots, the first C in slot order (token-major: first come,
+ *            first served); the other slots are dropped and add nothing to
+ *            their token's output (the kept weights are not renormalised).
+ *            Shared experts are never capped.  ("switchyard" page, 03 Load
+ *            balance, "What dropping tokens costs": capacity limits drop the
+ *            tokens an expert has no room for.)
  *   w8     : symmetric per-output-channel int8 weight-only quantisation,
  *            scale = max|row| / 127 (fp32), q = clamp(rint(W/scale), +-127);
  *            dequantised weight = (float)q * scale (fp32 product).
@@ -142,6 +149,54 @@ int oracle_permute(const int32_t *ids, int64_t T, int E, int S, int k, int32_t *
     return rc;
 }
 
+/* The dropping variant: expert e keeps its first `capacity` slots in slot
+ * order.  Layout: the kept routed rows by expert ([0, kept)), then the S
+ * shared groups of T rows.  sorted_slot[r] for r >= kept is -1; a dropped
+ * slot's row_of_slot is -2; *dropped = number of dropped slots. */
+int oracle_permute_capped(const int32_t *ids, int64_t T, int E, int S, int k, int64_t capacity,
+                          int32_t *offsets, int32_t *sorted_slot, int32_t *row_of_slot,
+                          int64_t *dropped) {
+    if (!ids || !offsets || !dropped || T < 0 || E < 1 || S < 0 || k < 1 || capacity < 0)
+        return OR_BAD_ARG;
+    const int64_t n = T * k;
+    if (n > 0 && (!sorted_slot || !row_of_slot)) return OR_BAD_ARG;
+    int64_t *count = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    int64_t *seen = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    if (!count || !seen) { free(count); free(seen); return OR_BAD_ARG; }
+    int rc = OR_OK;
+    for (int64_t s = 0; s < n; ++s) {
+        int32_t e = ids[s];
+        if (e < 0 || e >= E) { rc = OR_BAD_VALUE; break; }
+        count[e] += 1;
+    }
+    if (rc == OR_OK) {
+        offsets[0] = 0;
+        for (int e = 0; e < E; ++e) {
+            const int64_t kept = count[e] < capacity ? count[e] : capacity;
+            offsets[e + 1] = (int32_t)(offsets[e] + kept);
+        }
+        for (int s = 0; s < S; ++s) offsets[E + s + 1] = (int32_t)(offsets[E + s] + T);
+        for (int64_t r = 0; r < n; ++r) sorted_slot[r] = -1;
+        int64_t drops = 0;
+        for (int64_t s = 0; s < n; ++s) {
+            const int32_t e = ids[s];
+            const int64_t rank = seen[e]++;          /* earlier slots of expert e */
+            if (rank < capacity) {
+                const int64_t r = offsets[e] + rank;
+                sorted_slot[r] = (int32_t)s;
+                row_of_slot[s] = (int32_t)r;
+            } else {
+                row_of_slot[s] = -2;
+                drops += 1;
+            }
+        }
+        *dropped = drops;
+    }
+    free(count);
+    free(seen);
+    return rc;
+}
+
 /* ------------------------------------------------------------ expert FFN */
 
 /* h[i] = silu(sum_k Wg[i,k] x[k]) * (sum_k Wu[i,k] x[k]); Wg = rows 0..I-1 of
@@ -223,7 +278,7 @@ static void expert_ffn(const weights_t *W, int e, const double *x, int H, int I,
 static int layer_impl(const void *x, int x_is_f32, const int32_t *ids, const double *w,
                       int64_t T, int H, int E, int S, int k, int I, const weights_t *W,
                       const uint16_t *residual, const int64_t *tokens, int64_t ntok, double *y,
-                      int nthreads) {
+                      int nthreads, const unsigned char *keep) {
     if (!x || !ids || !w || !y || T < 0 || H < 1 || E < 1 || S < 0 || k < 1 || I < 1)
         return OR_BAD_ARG;
     const int64_t nout = tokens ? ntok : T;
@@ -252,6 +307,7 @@ static int layer_impl(const void *x, int x_is_f32, const int32_t *ids, const dou
                                  : bf16_value(((const uint16_t *)x)[t * H + c]);
             for (int c = 0; c < H; ++c) yt[c] = 0.0;
             for (int j = 0; j < k; ++j) {
+                if (keep && !keep[t * k + j]) continue;      /* dropped slot */
                 expert_ffn(W, ids[t * k + j], xv, H, I, h, fe);
                 for (int c = 0; c < H; ++c) yt[c] += w[t * k + j] * fe[c];
             }
@@ -277,7 +333,7 @@ int oracle_moe_layer(const void *x, int x_is_f32, const int32_t *ids, const doub
     if (!w_gu || !w_down) return OR_BAD_ARG;
     weights_t W = {w_gu, w_down, NULL, NULL, NULL, NULL};
     return layer_impl(x, x_is_f32, ids, w, T, H, E, S, k, I, &W, residual, tokens, ntok, y,
-                      nthreads);
+                      nthreads, NULL);
 }
 
 int oracle_moe_layer_w8(const void *x, int x_is_f32, const int32_t *ids, const double *w,
@@ -288,7 +344,37 @@ int oracle_moe_layer_w8(const void *x, int x_is_f32, const int32_t *ids, const d
     if (!q_gu || !s_gu || !q_down || !s_down) return OR_BAD_ARG;
     weights_t W = {NULL, NULL, q_gu, q_down, s_gu, s_down};
     return layer_impl(x, x_is_f32, ids, w, T, H, E, S, k, I, &W, residual, tokens, ntok, y,
-                      nthreads);
+                      nthreads, NULL);
+}
+
+/* The layer with capacity-limited experts: slot s = t*k + j is kept when
+ * fewer than `capacity` earlier slots (in slot order) chose the same expert;
+ * a dropped slot contributes nothing. */
+int oracle_moe_layer_capped(const void *x, int x_is_f32, const int32_t *ids, const double *w,
+                            int64_t T, int H, int E, int S, int k, int I, int64_t capacity,
+                            const uint16_t *w_gu, const uint16_t *w_down,
+                            const uint16_t *residual, const int64_t *tokens, int64_t ntok,
+                            double *y, int nthreads) {
+    if (!w_gu || !w_down || !ids || capacity < 0 || T < 0 || E < 1 || k < 1) return OR_BAD_ARG;
+    const int64_t n = T * k;
+    unsigned char *keep = (unsigned char *)malloc((size_t)(n > 0 ? n : 1));
+    int64_t *seen = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    if (!keep || !seen) { free(keep); free(seen); return OR_BAD_ARG; }
+    int rc = OR_OK;
+    for (int64_t s = 0; s < n; ++s) {
+        const int32_t e = ids[s];
+        if (e < 0 || e >= E) { rc = OR_BAD_VALUE; break; }
+        keep[s] = seen[e] < capacity;
+        seen[e] += 1;
+    }
+    if (rc == OR_OK) {
+        weights_t W = {w_gu, w_down, NULL, NULL, NULL, NULL};
+        rc = layer_impl(x, x_is_f32, ids, w, T, H, E, S, k, I, &W, residual, tokens, ntok, y,
+                        nthreads, keep);
+    }
+    free(keep);
+    free(seen);
+    return rc;
 }
 
 /* ------------------------------------------------------------- quantise */

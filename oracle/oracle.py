@@ -45,6 +45,9 @@ def load():
             sigs = {
                 "oracle_route": [P, I64, I32, I32, I32, P, P],
                 "oracle_permute": [P, I64, I32, I32, I32, P, P, P],
+                "oracle_permute_capped": [P, I64, I32, I32, I32, I64, P, P, P, P],
+                "oracle_moe_layer_capped": [P, I32, P, P, I64, I32, I32, I32, I32, I32, I64, P,
+                                            P, P, P, I64, P, I32],
                 "oracle_expert_hidden": [P, P, I32, I32, P],
                 "oracle_expert_down": [P, P, I32, I32, P],
                 "oracle_moe_layer": [P, I32, P, P, I64, I32, I32, I32, I32, I32, P, P, P, P, I64,
@@ -107,6 +110,22 @@ def permute(ids, E: int, S: int = 0):
     return off, ss, ros
 
 
+def permute_capped(ids, E: int, S: int, capacity: int):
+    """The dropping variant: each routed expert keeps its first `capacity`
+    slots in slot order.  Returns (offsets int32 [E+S+1], sorted_slot int32
+    [T*k] (-1 past the kept rows), row_of_slot int32 [T*k] (-2: dropped),
+    dropped: int)."""
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    off = np.empty(E + S + 1, np.int32)
+    ss = np.empty(T * k, np.int32)
+    ros = np.empty(T * k, np.int32)
+    dropped = ctypes.c_int64(0)
+    _check(load().oracle_permute_capped(_p(ids), T, E, S, k, int(capacity), _p(off), _p(ss),
+                                        _p(ros), ctypes.byref(dropped)), "permute_capped")
+    return off, ss, ros, int(dropped.value)
+
+
 def expert_hidden(x_row, w_gu_e_bits, H: int, I: int):
     """h = silu(Wg x) * (Wu x) for one expert; w_gu_e_bits: uint16 [2I, H]."""
     x = _c(x_row, np.float64)
@@ -132,10 +151,11 @@ def _x_args(x):
 
 
 def moe_layer(x, ids, w, E: int, S: int, w_gu_bits, w_down_bits, residual_bits=None,
-              tokens=None, nthreads: int = 0):
+              tokens=None, nthreads: int = 0, capacity=None):
     """Full MoE layer in fp64.  x: float32 [T,H] or bf16 bits uint16 [T,H];
     w_gu_bits uint16 [E+S, 2I, H]; w_down_bits uint16 [E+S, H, I].
-    Returns float64 [T or len(tokens), H]."""
+    capacity: None (dropless) or the per-expert slot capacity of the
+    dropping variant.  Returns float64 [T or len(tokens), H]."""
     xa, xf = _x_args(x)
     T, H = xa.shape
     ids = _c(ids, np.int32)
@@ -150,9 +170,15 @@ def moe_layer(x, ids, w, E: int, S: int, w_gu_bits, w_down_bits, residual_bits=N
     tok = None if tokens is None else _c(tokens, np.int64)
     nout = T if tok is None else len(tok)
     y = np.empty((nout, H), np.float64)
-    _check(load().oracle_moe_layer(_p(xa), xf, _p(ids), _p(w), T, H, E, S, k, I, _p(wgu), _p(wd),
-                                   _p(res), _p(tok), 0 if tok is None else len(tok), _p(y),
-                                   nthreads), "moe_layer")
+    if capacity is None:
+        _check(load().oracle_moe_layer(_p(xa), xf, _p(ids), _p(w), T, H, E, S, k, I, _p(wgu),
+                                       _p(wd), _p(res), _p(tok), 0 if tok is None else len(tok),
+                                       _p(y), nthreads), "moe_layer")
+    else:
+        _check(load().oracle_moe_layer_capped(_p(xa), xf, _p(ids), _p(w), T, H, E, S, k, I,
+                                              int(capacity), _p(wgu), _p(wd), _p(res), _p(tok),
+                                              0 if tok is None else len(tok), _p(y), nthreads),
+               "moe_layer_capped")
     return y
 
 
