@@ -41,6 +41,8 @@ _SIGS = {
     "moe_route": ([P, I, I, I, I, P, P, P, P], I),
     "moe_permute_workspace_size": ([I, I, I, I], SZ),
     "moe_permute": ([P, I, I, I, I, P, I, I, P, P, P, P, P, SZ, P, P], I),
+    "moe_permute_capped": ([P, I, I, I, I, I, P, I, I, P, P, P, P, P, P, SZ, P, P], I),
+    "moe_combine_capped": ([P, P, P, P, I, I, I, I, I, P, P, P, P], I),
     "moe_ffn_workspace_size": ([I, I], SZ),
     "moe_grouped_gemm_swiglu": ([P, P, I, I, I, I, P, P, P, P, SZ, P, P], I),
     "moe_grouped_gemv": ([P, P, I, I, I, I, P, P, P, P, SZ, P, P], I),
@@ -156,6 +158,40 @@ def moe_permute(topk_ids, E, S, x, offsets, sorted_slot, row_of_slot, x_perm, wo
     _ok(_lib.moe_permute(_ptr(topk_ids), T, E, S, k, _ptr(x), xd, H, _ptr(offsets),
                          _ptr(sorted_slot), _ptr(row_of_slot), _ptr(x_perm), _ptr(workspace),
                          wsb, _ptr(dev_error), _stream(stream)), "moe_permute")
+
+
+MOE_ROW_DROPPED = -2
+
+
+def capacity_of(capacity_factor: float, T: int, k: int, E: int) -> int:
+    """Slots per routed expert for a capacity factor: ceil(CF * T*k / E)."""
+    import math
+    return int(math.ceil(capacity_factor * T * k / E))
+
+
+def moe_permute_capped(topk_ids, E, S, capacity, x, offsets, sorted_slot, row_of_slot, x_perm,
+                       dropped, workspace=None, dev_error=None, stream=None):
+    """moe_permute with at most `capacity` slots per routed expert (the first
+    in slot order); dropped: int32 [1] device tensor <- number of dropped slots."""
+    _dev(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    _dev(x, "x")
+    if x.dtype == torch.bfloat16:
+        xd = MOE_DTYPE_BF16
+    elif x.dtype == torch.float32:
+        xd = MOE_DTYPE_F32
+    else:
+        raise ValueError("x must be bf16 or fp32")
+    H = x.shape[1]
+    for n, t in (("offsets", offsets), ("sorted_slot", sorted_slot),
+                 ("row_of_slot", row_of_slot), ("dropped", dropped)):
+        _dev(t, n, torch.int32)
+    _dev(x_perm, "x_perm", torch.bfloat16)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(_lib.moe_permute_capped(_ptr(topk_ids), T, E, S, k, int(capacity), _ptr(x), xd, H,
+                                _ptr(offsets), _ptr(sorted_slot), _ptr(row_of_slot),
+                                _ptr(x_perm), _ptr(dropped), _ptr(workspace), wsb,
+                                _ptr(dev_error), _stream(stream)), "moe_permute_capped")
 
 
 ROUTE_PERMUTE_MAX_SLOTS = 1024
@@ -301,6 +337,22 @@ def moe_combine(y_perm, row_of_slot, topk_w, S, out, residual=None, dev_error=No
     _ok(_lib.moe_combine(_ptr(y_perm), _ptr(row_of_slot), _ptr(topk_w), T, k, S, H,
                          _ptr(residual), _ptr(out), _ptr(dev_error), _stream(stream)),
         "moe_combine")
+
+
+def moe_combine_capped(y_perm, row_of_slot, topk_w, offsets, E, S, out, residual=None,
+                       dev_error=None, stream=None):
+    """moe_combine after moe_permute_capped (dropped slots add nothing; the
+    shared rows start at offsets[E])."""
+    _dev(y_perm, "y_perm", torch.bfloat16); _dev(row_of_slot, "row_of_slot", torch.int32)
+    _dev(topk_w, "topk_w", torch.float32); _dev(out, "out", torch.bfloat16)
+    _dev(offsets, "offsets", torch.int32)
+    if residual is not None:
+        _dev(residual, "residual", torch.bfloat16)
+    T, k = topk_w.shape
+    H = out.shape[1]
+    _ok(_lib.moe_combine_capped(_ptr(y_perm), _ptr(row_of_slot), _ptr(topk_w), _ptr(offsets), E,
+                                T, k, S, H, _ptr(residual), _ptr(out), _ptr(dev_error),
+                                _stream(stream)), "moe_combine_capped")
 
 
 def moe_quantize_w8(w: torch.Tensor):

@@ -14,8 +14,8 @@ constexpr int CB_CPT = 2;             // 8-element chunks per thread
 
 __global__ void __launch_bounds__(256) combine_kernel(
     const uint16_t *__restrict__ y_perm, const int32_t *__restrict__ row_of_slot,
-    const float *__restrict__ topk_w, int T, int k, int S, int H,
-    const uint16_t *residual, uint16_t *out, int32_t *dev_error) {
+    const float *__restrict__ topk_w, const int32_t *__restrict__ offsets, int E, int T, int k,
+    int S, int H, const uint16_t *residual, uint16_t *out, int32_t *dev_error) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.y;
@@ -23,6 +23,14 @@ __global__ void __launch_bounds__(256) combine_kernel(
     const int chunks = H / 8;
     if (c0 >= chunks) return;
     const int64_t n = static_cast<int64_t>(T) * k;
+    // shared rows follow the routed rows: at n (dropless) or after the
+    // served routed rows (capacity-limited permute: offsets[E])
+    int64_t shared0 = offsets ? static_cast<int64_t>(offsets[E]) : n;
+    if (shared0 < 0 || shared0 > n) {            // inconsistent offsets: skip the shared rows
+        if (S > 0) report(dev_error, MOE_ERR_DEVICE_CHECK);
+        shared0 = 0;
+        S = 0;
+    }
     float acc[CB_CPT][8];
 #pragma unroll
     for (int q = 0; q < CB_CPT; ++q)
@@ -51,7 +59,8 @@ __global__ void __launch_bounds__(256) combine_kernel(
                 r[j] = row_of_slot[slot];
                 w[j] = topk_w[slot];
                 ok[j] = r[j] >= 0 && r[j] < n;
-                if (!ok[j]) report(dev_error, MOE_ERR_DEVICE_CHECK);
+                // a slot dropped by the capacity limit adds nothing
+                if (!ok[j] && r[j] != MOE_ROW_DROPPED) report(dev_error, MOE_ERR_DEVICE_CHECK);
             }
         }
         uint4 v[BATCH][CB_CPT];
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
 #pragma unroll
             for (int q = 0; q < CB_CPT; ++q)
                 if (s0 + j < S && c0 + q < chunks)
-                    v[j][q] = ld_nc(y_perm + (n + static_cast<int64_t>(s0 + j) * T + t) * H +
+                    v[j][q] = ld_nc(y_perm + (shared0 + static_cast<int64_t>(s0 + j) * T + t) * H +
                                     (c0 + q) * 8);
 #pragma unroll
         for (int j = 0; j < BATCH; ++j)
@@ -107,10 +116,11 @@ __global__ void __launch_bounds__(256) combine_kernel(
 
 using namespace moe;
 
-extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_slot,
-                                  const float *topk_w, int T, int k, int S, int H,
-                                  const uint16_t *residual, uint16_t *out, int32_t *dev_error,
-                                  cudaStream_t stream) {
+namespace moe {
+static moe_status combine_impl(const uint16_t *y_perm, const int32_t *row_of_slot,
+                               const float *topk_w, const int32_t *offsets, int E, int T, int k,
+                               int S, int H, const uint16_t *residual, uint16_t *out,
+                               int32_t *dev_error, cudaStream_t stream) {
     if (!y_perm || !row_of_slot || !topk_w || !out || T < 1 || k < 1 || k > 32 || S < 0 || H < 1)
         return MOE_ERR_INVALID_ARG;
     const int64_t M = static_cast<int64_t>(T) * k + static_cast<int64_t>(S) * T;
@@ -122,7 +132,26 @@ extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_
     const int per_thread = (chunks + CB_CPT - 1) / CB_CPT;
     const int threads = per_thread >= 128 ? 128 : ((per_thread + 31) / 32) * 32;
     dim3 grid((per_thread + threads - 1) / threads, T);
-    launch(combine_kernel, grid, threads, 0, stream, y_perm, row_of_slot, topk_w, T, k, S, H, residual,
-                                                 out, dev_error);
+    launch(combine_kernel, grid, threads, 0, stream, y_perm, row_of_slot, topk_w, offsets, E, T, k,
+           S, H, residual, out, dev_error);
     return launch_status();
+}
+}  // namespace moe
+
+extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_slot,
+                                  const float *topk_w, int T, int k, int S, int H,
+                                  const uint16_t *residual, uint16_t *out, int32_t *dev_error,
+                                  cudaStream_t stream) {
+    return combine_impl(y_perm, row_of_slot, topk_w, nullptr, 0, T, k, S, H, residual, out,
+                        dev_error, stream);
+}
+
+extern "C" moe_status moe_combine_capped(const uint16_t *y_perm, const int32_t *row_of_slot,
+                                         const float *topk_w, const int32_t *offsets, int E,
+                                         int T, int k, int S, int H, const uint16_t *residual,
+                                         uint16_t *out, int32_t *dev_error,
+                                         cudaStream_t stream) {
+    if (!offsets || E < 1) return MOE_ERR_INVALID_ARG;
+    return combine_impl(y_perm, row_of_slot, topk_w, offsets, E, T, k, S, H, residual, out,
+                        dev_error, stream);
 }

@@ -21,6 +21,7 @@
 //    copies the rows.  Three launches, each spread over the GPU;
 //  * moe_route_permute also routes, inside the small kernel.
 #include <algorithm>
+#include <climits>
 
 #include "route_token.cuh"
 
@@ -118,7 +119,8 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
     const int32_t *__restrict__ ids_in, const float *__restrict__ logits, int renormalize, int T,
     int E, int S, int k, const void *__restrict__ x, int H, int32_t *__restrict__ topk_ids,
     float *__restrict__ topk_w, int32_t *__restrict__ offsets, int32_t *__restrict__ sorted_slot,
-    int32_t *__restrict__ row_of_slot, uint16_t *__restrict__ x_perm, int32_t *dev_error) {
+    int32_t *__restrict__ row_of_slot, uint16_t *__restrict__ x_perm, int cap,
+    int32_t *__restrict__ dropped, int32_t *dev_error) {
     extern __shared__ int smem[];
     int *s_cnt = smem;                          // [32][E]
     int *s_base = smem + 32 * E;                // [E+1]
@@ -166,24 +168,35 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
         return;
     }
     const int rank = block_rank(e, E, s_cnt, s_base);
-    if (tid < 32) warp_exclusive_scan_inplace(s_base, E);
+    // an expert serves at most `cap` slots (all of them in the dropless call)
+    for (int g = tid; g <= E; g += blockDim.x) s_base[g] = g < E ? min(s_base[g], cap) : 0;
     __syncthreads();
-    if (blockIdx.x == 0)
+    if (tid < 32) warp_exclusive_scan_inplace(s_base, E + 1);
+    __syncthreads();
+    const int kept = s_base[E];                 // routed rows; shared rows follow
+    if (blockIdx.x == 0) {
         for (int g = tid; g <= E + S; g += blockDim.x)
-            offsets[g] = g < E ? s_base[g] : n + (g - E) * T;
+            offsets[g] = g <= E ? s_base[g] : kept + (g - E) * T;
+        for (int r = kept + tid; r < n; r += blockDim.x) sorted_slot[r] = -1;
+        if (tid == 0 && dropped) *dropped = n - kept;
+    }
     if (e >= 0) {
-        const int pos = s_base[e] + rank;
-        s_sorted[pos] = tid;
-        if (blockIdx.x == 0) {
-            sorted_slot[pos] = tid;
-            row_of_slot[tid] = pos;
+        if (rank < cap) {
+            const int pos = s_base[e] + rank;
+            s_sorted[pos] = tid;
+            if (blockIdx.x == 0) {
+                sorted_slot[pos] = tid;
+                row_of_slot[tid] = pos;
+            }
+        } else if (blockIdx.x == 0) {
+            row_of_slot[tid] = MOE_ROW_DROPPED;
         }
     }
     __syncthreads();
-    const int M = n + S * T;
+    const int M = kept + S * T;
     const int warps = blockDim.x >> 5;
     for (int r = blockIdx.x * warps + (tid >> 5); r < M; r += gridDim.x * warps) {
-        const int t = r < n ? s_sorted[r] / k : (r - n) % T;
+        const int t = r < kept ? s_sorted[r] / k : (r - kept) % T;
         copy_row<X_F32>(x, t, H, x_perm + static_cast<int64_t>(r) * H);
     }
 }
@@ -216,7 +229,9 @@ __global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t *__re
 }
 
 // Dynamic shared memory of the placing kernel: ranking area + bases [E].
-inline size_t place_smem_bytes(int E) { return rank_smem_bytes(E) + static_cast<size_t>(E) * 4; }
+inline size_t place_smem_bytes(int E) {
+    return rank_smem_bytes(E) + static_cast<size_t>(2 * E + 1) * 4;
+}
 
 // Places chunk blockIdx.x.  The base of expert g in this chunk is g's offset
 // (scan of all chunks' totals) plus g's count in earlier chunks; CTA 0 also
@@ -224,11 +239,12 @@ inline size_t place_smem_bytes(int E) { return rank_smem_bytes(E) + static_cast<
 __global__ void __launch_bounds__(1024) permute_place_kernel(
     const int32_t *__restrict__ ids, int T, int E, int S, int k, const int32_t *__restrict__ counts,
     int nchunks, int32_t *__restrict__ offsets, int32_t *__restrict__ sorted_slot,
-    int32_t *__restrict__ row_of_slot) {
+    int32_t *__restrict__ row_of_slot, int cap, int32_t *__restrict__ dropped) {
     extern __shared__ int smem[];
     int *s_cnt = smem;                           // [32][E], zero until the ranking
     int *s_tot = smem + 32 * E;                  // [E+1]
     int *s_base = s_tot + E + 1;                 // [E]
+    int *s_off = s_base + E;                     // [E+1]
     __shared__ int s_bad;
     const int64_t n = static_cast<int64_t>(T) * k;
     const int c = blockIdx.x;
@@ -254,21 +270,31 @@ __global__ void __launch_bounds__(1024) permute_place_kernel(
         if (c == 0) write_empty(E, S, n, offsets, row_of_slot);
         return;
     }
-    if (threadIdx.x < 32) warp_exclusive_scan_inplace(s_tot, E);
+    // offsets: exclusive scan of the served counts min(total, cap)
+    for (int g = threadIdx.x; g <= E; g += blockDim.x) s_off[g] = g < E ? min(s_tot[g], cap) : 0;
     __syncthreads();
-    if (c == 0)
+    if (threadIdx.x < 32) warp_exclusive_scan_inplace(s_off, E + 1);
+    __syncthreads();
+    const int64_t kept = s_off[E];               // routed rows; shared rows follow
+    if (c == 0) {
         for (int g = threadIdx.x; g <= E + S; g += blockDim.x)
-            offsets[g] = g < E ? s_tot[g]
-                               : static_cast<int32_t>(n + static_cast<int64_t>(g - E) * T);
-    for (int g = threadIdx.x; g < E; g += blockDim.x) s_base[g] += s_tot[g];
-    __syncthreads();
+            offsets[g] = g <= E ? s_off[g]
+                                : static_cast<int32_t>(kept + static_cast<int64_t>(g - E) * T);
+        if (threadIdx.x == 0 && dropped) *dropped = static_cast<int32_t>(n - kept);
+    }
     const int64_t s = static_cast<int64_t>(c) * CHUNK + threadIdx.x;
+    if (s >= kept && s < n) sorted_slot[s] = -1;     // positions past the served rows
     const int e = s < n ? ids[s] : -1;
     const int rank = block_rank(e, E, s_cnt, s_tot);
     if (e >= 0) {
-        const int pos = s_base[e] + rank;
-        sorted_slot[pos] = static_cast<int32_t>(s);
-        row_of_slot[s] = pos;
+        const int grank = s_base[e] + rank;      // earlier chunks' slots of e + this chunk's
+        if (grank < cap) {
+            const int pos = s_off[e] + grank;
+            sorted_slot[pos] = static_cast<int32_t>(s);
+            row_of_slot[s] = pos;
+        } else {
+            row_of_slot[s] = MOE_ROW_DROPPED;
+        }
     }
 }
 
@@ -281,20 +307,18 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(
     pdl_wait();
     pdl_trigger();
     const int64_t n = static_cast<int64_t>(T) * k;
-    const int64_t M = n + static_cast<int64_t>(S) * T;
-    const int64_t routed_rows = offsets[E];      // 0 after an invalid routing
+    const int64_t routed_rows = offsets[E];      // served routed rows
+    const int64_t M = offsets[E + S];            // all rows; 0 after an invalid routing
     const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < M;
          r += wstride) {
         int64_t t;
-        if (r < n) {
-            if (r >= routed_rows) continue;
+        if (r < routed_rows) {
             const int64_t s = sorted_slot[r];
             if (s < 0 || s >= n) continue;
             t = s / k;
         } else {
-            if (routed_rows != n) continue;
-            t = (r - n) % T;
+            t = (r - routed_rows) % T;
         }
         copy_row<X_F32>(x, t, H, x_perm + r * H);
     }
@@ -323,7 +347,8 @@ static moe_status launch_small(bool x_f32, const int32_t *ids, const float *logi
                                int renormalize, int T, int E, int S, int k, const void *x, int H,
                                int32_t *topk_ids, float *topk_w, int32_t *offsets,
                                int32_t *sorted_slot, int32_t *row_of_slot, uint16_t *x_perm,
-                               int32_t *dev_error, cudaStream_t stream) {
+                               int cap, int32_t *dropped, int32_t *dev_error,
+                               cudaStream_t stream) {
     const int64_t M = static_cast<int64_t>(T) * k + static_cast<int64_t>(S) * T;
     const int grid = static_cast<int>(std::min<int64_t>((M + 31) / 32, sm_count()));
     const size_t smem = rank_smem_bytes(E);
@@ -332,12 +357,14 @@ static moe_status launch_small(bool x_f32, const int32_t *ids, const float *logi
         auto kern = permute_small_kernel<ROUTE, PER_LANE, true>;
         if (!allow_smem(kern, smem, done_f32)) return MOE_ERR_UNSUPPORTED;
         launch(kern, grid, CHUNK, smem, stream, ids, logits, renormalize, T, E, S, k, x, H,
-               topk_ids, topk_w, offsets, sorted_slot, row_of_slot, x_perm, dev_error);
+               topk_ids, topk_w, offsets, sorted_slot, row_of_slot, x_perm, cap, dropped,
+               dev_error);
     } else {
         auto kern = permute_small_kernel<ROUTE, PER_LANE, false>;
         if (!allow_smem(kern, smem, done_bf16)) return MOE_ERR_UNSUPPORTED;
         launch(kern, grid, CHUNK, smem, stream, ids, logits, renormalize, T, E, S, k, x, H,
-               topk_ids, topk_w, offsets, sorted_slot, row_of_slot, x_perm, dev_error);
+               topk_ids, topk_w, offsets, sorted_slot, row_of_slot, x_perm, cap, dropped,
+               dev_error);
     }
     return launch_status();
 }
@@ -356,14 +383,18 @@ extern "C" size_t moe_permute_workspace_size(int T, int E, int S, int k) {
     return (bytes + 255) & ~static_cast<size_t>(255);
 }
 
-extern "C" moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, int k,
-                                  const void *x, int x_dtype, int H, int32_t *offsets,
-                                  int32_t *sorted_slot, int32_t *row_of_slot, uint16_t *x_perm,
-                                  void *workspace, size_t workspace_bytes, int32_t *dev_error,
-                                  cudaStream_t stream) {
+namespace moe {
+// moe_permute and moe_permute_capped: cap = slots an expert may serve
+// (INT_MAX: all), dropped = device word for the dropped-slot count or NULL.
+static moe_status permute_impl(const int32_t *topk_ids, int T, int E, int S, int k, int cap,
+                               const void *x, int x_dtype, int H, int32_t *offsets,
+                               int32_t *sorted_slot, int32_t *row_of_slot, uint16_t *x_perm,
+                               int32_t *dropped, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_error, cudaStream_t stream) {
     if (!topk_ids || !x || !offsets || !sorted_slot || !row_of_slot || !x_perm)
         return MOE_ERR_INVALID_ARG;
-    if (T < 1 || E < 1 || S < 0 || k < 1 || k > E || k > 32 || H < 1) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || E < 1 || S < 0 || k < 1 || k > E || k > 32 || H < 1 || cap < 0)
+        return MOE_ERR_INVALID_ARG;
     if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
     if (E + S > 1024) return MOE_ERR_UNSUPPORTED;
     const int64_t n = static_cast<int64_t>(T) * k, M = n + static_cast<int64_t>(S) * T;
@@ -372,8 +403,8 @@ extern "C" moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, 
     const bool f32 = x_dtype == MOE_DTYPE_F32;
     if (n <= CHUNK)
         return launch_small<false, 1>(f32, topk_ids, nullptr, 0, T, E, S, k, x, H, nullptr,
-                                      nullptr, offsets, sorted_slot, row_of_slot, x_perm,
-                                      dev_error, stream);
+                                      nullptr, offsets, sorted_slot, row_of_slot, x_perm, cap,
+                                      dropped, dev_error, stream);
 
     const size_t need = moe_permute_workspace_size(T, E, S, k);
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
@@ -389,7 +420,8 @@ extern "C" moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, 
     moe_status st = launch_status();
     if (st != MOE_OK) return st;
     launch(permute_place_kernel, nchunks, CHUNK, place_smem_bytes(E), stream, topk_ids, T, E, S,
-           k, static_cast<const int32_t *>(counts), nchunks, offsets, sorted_slot, row_of_slot);
+           k, static_cast<const int32_t *>(counts), nchunks, offsets, sorted_slot, row_of_slot,
+           cap, dropped);
     if ((st = launch_status()) != MOE_OK) return st;
     const int blocks = static_cast<int>(std::min<int64_t>((M + 7) / 8, sm_count() * 8ll));
     if (f32)
@@ -401,6 +433,30 @@ extern "C" moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, 
                static_cast<const int32_t *>(offsets), static_cast<const int32_t *>(sorted_slot),
                x_perm);
     return launch_status();
+}
+}  // namespace moe
+
+extern "C" moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, int k,
+                                  const void *x, int x_dtype, int H, int32_t *offsets,
+                                  int32_t *sorted_slot, int32_t *row_of_slot, uint16_t *x_perm,
+                                  void *workspace, size_t workspace_bytes, int32_t *dev_error,
+                                  cudaStream_t stream) {
+    return permute_impl(topk_ids, T, E, S, k, INT_MAX, x, x_dtype, H, offsets, sorted_slot,
+                        row_of_slot, x_perm, nullptr, workspace, workspace_bytes, dev_error,
+                        stream);
+}
+
+extern "C" moe_status moe_permute_capped(const int32_t *topk_ids, int T, int E, int S, int k,
+                                         int capacity, const void *x, int x_dtype, int H,
+                                         int32_t *offsets, int32_t *sorted_slot,
+                                         int32_t *row_of_slot, uint16_t *x_perm,
+                                         int32_t *dropped, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_error,
+                                         cudaStream_t stream) {
+    if (!dropped) return MOE_ERR_INVALID_ARG;
+    return permute_impl(topk_ids, T, E, S, k, capacity, x, x_dtype, H, offsets, sorted_slot,
+                        row_of_slot, x_perm, dropped, workspace, workspace_bytes, dev_error,
+                        stream);
 }
 
 extern "C" moe_status moe_route_permute(const float *logits, int T, int E, int S, int k,
@@ -424,16 +480,16 @@ extern "C" moe_status moe_route_permute(const float *logits, int T, int E, int S
     if (per_lane <= 1)
         return launch_small<true, 1>(f32, nullptr, logits, renormalize, T, E, S, k, x, H,
                                      topk_ids, topk_w, offsets, sorted_slot, row_of_slot, x_perm,
-                                     dev_error, stream);
+                                     INT_MAX, nullptr, dev_error, stream);
     if (per_lane <= 2)
         return launch_small<true, 2>(f32, nullptr, logits, renormalize, T, E, S, k, x, H,
                                      topk_ids, topk_w, offsets, sorted_slot, row_of_slot, x_perm,
-                                     dev_error, stream);
+                                     INT_MAX, nullptr, dev_error, stream);
     if (per_lane <= 4)
         return launch_small<true, 4>(f32, nullptr, logits, renormalize, T, E, S, k, x, H,
                                      topk_ids, topk_w, offsets, sorted_slot, row_of_slot, x_perm,
-                                     dev_error, stream);
+                                     INT_MAX, nullptr, dev_error, stream);
     return launch_small<true, 8>(f32, nullptr, logits, renormalize, T, E, S, k, x, H, topk_ids,
-                                 topk_w, offsets, sorted_slot, row_of_slot, x_perm, dev_error,
-                                 stream);
+                                 topk_w, offsets, sorted_slot, row_of_slot, x_perm, INT_MAX,
+                                 nullptr, dev_error, stream);
 }

@@ -32,6 +32,8 @@ class LayerBuffers:
     ffn_ws: torch.Tensor
     perm_ws: torch.Tensor | None
     out: torch.Tensor
+    dropped: torch.Tensor            # int32 [1]: slots dropped by the capacity limit
+    capacity: int | None             # slots per routed expert, or None (dropless)
 
 
 class MoELayer:
@@ -44,10 +46,14 @@ class MoELayer:
     """
 
     def __init__(self, H, E, k, I, S=0, renormalize=False, w_gu=None, w_down=None,
-                 q_gu=None, s_gu=None, q_down=None, s_down=None, device="cuda"):
+                 q_gu=None, s_gu=None, q_down=None, s_down=None, device="cuda",
+                 capacity_factor=None):
         self.H, self.E, self.k, self.I, self.S = H, E, k, I, S
         self.G = E + S
         self.renormalize = bool(renormalize)
+        # None: dropless; else each routed expert serves at most
+        # ceil(capacity_factor * T*k / E) slots per batch (the rest are dropped)
+        self.capacity_factor = capacity_factor
         self.device = torch.device(device)
         self.int8 = q_gu is not None
         if self.int8:
@@ -81,6 +87,9 @@ class MoELayer:
                 ffn_ws=torch.empty(max(ws, 256), dtype=torch.uint8, device=d),
                 perm_ws=(torch.empty(pws, dtype=torch.uint8, device=d) if pws else None),
                 out=torch.empty((T, self.H), dtype=torch.bfloat16, device=d),
+                dropped=torch.zeros(1, dtype=torch.int32, device=d),
+                capacity=(None if self.capacity_factor is None else
+                          B.capacity_of(self.capacity_factor, T, self.k, self.E)),
             )
             self._bufs[T] = b
         return b
@@ -92,6 +101,11 @@ class MoELayer:
         B.moe_route(logits, self.k, self.renormalize, b.topk_ids, b.topk_w, self.err, stream)
 
     def permute(self, x, b: LayerBuffers, stream=None):
+        if b.capacity is not None:
+            B.moe_permute_capped(b.topk_ids, self.E, self.S, b.capacity, x, b.offsets,
+                                 b.sorted_slot, b.row_of_slot, b.x_perm, b.dropped, b.perm_ws,
+                                 self.err, stream)
+            return
         B.moe_permute(b.topk_ids, self.E, self.S, x, b.offsets, b.sorted_slot, b.row_of_slot,
                       b.x_perm, b.perm_ws, self.err, stream)
 
@@ -99,7 +113,7 @@ class MoELayer:
         # the fused kernel routes every token in every CTA, one warp per token:
         # worth it while a CTA's 32 warps route each token at most once
         return (T <= 32 and T * self.k <= B.ROUTE_PERMUTE_MAX_SLOTS
-                and self.E <= B.ROUTE_PERMUTE_MAX_E)
+                and self.E <= B.ROUTE_PERMUTE_MAX_E and self.capacity_factor is None)
 
     def route_permute(self, logits, x, b: LayerBuffers, stream=None):
         """Routing and permutation: one fused launch for decode-sized batches,
@@ -137,6 +151,10 @@ class MoELayer:
             fn(b.x_perm, b.offsets, self.w_gu, self.w_down, b.y_perm, b.ffn_ws, self.err, stream)
 
     def combine(self, b: LayerBuffers, out, residual=None, stream=None):
+        if b.capacity is not None:
+            B.moe_combine_capped(b.y_perm, b.row_of_slot, b.topk_w, b.offsets, self.E, self.S,
+                                 out, residual, self.err, stream)
+            return
         B.moe_combine(b.y_perm, b.row_of_slot, b.topk_w, self.S, out, residual, self.err, stream)
 
     def forward(self, x, logits, out=None, residual=None, ffn="auto", stream=None):

@@ -65,6 +65,10 @@ typedef enum moe_status {
 
 typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
 
+/* row_of_slot value of a slot that moe_permute_capped dropped (its expert
+ * had no room left); moe_combine_capped adds nothing for it. */
+#define MOE_ROW_DROPPED (-2)
+
 /* Static description of a status code; never NULL. */
 const char *moe_status_string(int status);
 
@@ -124,6 +128,33 @@ moe_status moe_permute(const int32_t *topk_ids, int T, int E, int S, int k, cons
                        int x_dtype, int H, int32_t *offsets, int32_t *sorted_slot,
                        int32_t *row_of_slot, uint16_t *x_perm, void *workspace,
                        size_t workspace_bytes, int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * moe_permute_capped -- moe_permute with a capacity limit per routed expert,
+ * the token-dropping variant ("switchyard" page, 03 Load balance, "What
+ * dropping tokens costs": capacity limits drop the tokens an expert has no
+ * room for).  Routed expert e serves at most `capacity` of its slots: the
+ * first ones in slot order (t*k + j ascending: first come, first served);
+ * the others are dropped.  A capacity factor CF gives capacity =
+ * ceil(CF * T*k / E).  Shared experts are never capped.  Outputs as for
+ * moe_permute, except:
+ *   offsets     routed group e holds min(count_e, capacity) rows; the shared
+ *               groups start at offsets[E] (the served routed rows), so
+ *               offsets[G] = offsets[E] + S*T <= M;
+ *   sorted_slot entries at positions offsets[E] .. T*k-1 are -1;
+ *   row_of_slot MOE_ROW_DROPPED for a dropped slot;
+ *   x_perm      rows past offsets[G] are not written;
+ *   dropped     one int32 in device memory, set to the number of dropped
+ *               slots (T*k - offsets[E]); must not be NULL.
+ * capacity >= every expert's count gives exactly moe_permute's outputs.
+ * The FFN calls take the permuted row count M = T*k + S*T as before (an
+ * upper bound of the rows in use); combine with moe_combine_capped.
+ */
+moe_status moe_permute_capped(const int32_t *topk_ids, int T, int E, int S, int k, int capacity,
+                              const void *x, int x_dtype, int H, int32_t *offsets,
+                              int32_t *sorted_slot, int32_t *row_of_slot, uint16_t *x_perm,
+                              int32_t *dropped, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_error, cudaStream_t stream);
 
 /*
  * moe_route_permute -- moe_route followed by moe_permute in one launch, for
@@ -256,6 +287,21 @@ moe_status moe_grouped_gemv_noalloc(const uint16_t *x_perm, const int32_t *offse
 moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_slot, const float *topk_w,
                        int T, int k, int S, int H, const uint16_t *residual, uint16_t *out,
                        int32_t *dev_error, cudaStream_t stream);
+
+/*
+ * moe_combine_capped -- moe_combine after moe_permute_capped: a slot whose
+ * row_of_slot is MOE_ROW_DROPPED adds nothing (the kept weights are not
+ * renormalised), and the shared rows are read from offsets[E] + s*T + t.
+ *   out[t] = bf16( sum_{j<k, slot kept} topk_w[t,j] * y_perm[row_of_slot[t*k+j]]
+ *                  + sum_{s<S} y_perm[offsets[E] + s*T + t]  (+ residual[t]) )
+ * offsets: [E+S+1] from moe_permute_capped (read on the device; an
+ * offsets[E] outside [0, T*k] is a device-check fault and the shared rows
+ * are skipped).  Other arguments as for moe_combine.
+ */
+moe_status moe_combine_capped(const uint16_t *y_perm, const int32_t *row_of_slot,
+                              const float *topk_w, const int32_t *offsets, int E, int T, int k,
+                              int S, int H, const uint16_t *residual, uint16_t *out,
+                              int32_t *dev_error, cudaStream_t stream);
 
 /*
  * moe_quantize_w8 -- offline, host-side int8 quantisation of expert

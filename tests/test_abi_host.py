@@ -136,6 +136,23 @@ def test_router_logits_argument_checks(lib):
     assert f(ODD, GOOD, None, 4, 64, 8, GOOD, None) == 3
 
 
+def test_capped_permute_and_combine_argument_checks(lib):
+    f = lib.moe_permute_capped
+    f.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                  ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    assert f(GOOD, 4, 8, 0, 2, -1, GOOD, 0, 64, GOOD, GOOD, GOOD, GOOD, GOOD, None, 0, None,
+             None) == 1                                  # negative capacity
+    assert f(GOOD, 4, 8, 0, 2, 3, GOOD, 0, 64, GOOD, GOOD, GOOD, GOOD, None, None, 0, None,
+             None) == 1                                  # no dropped-count word
+    assert f(GOOD, 4, 8, 0, 2, 3, GOOD, 0, 60, GOOD, GOOD, GOOD, GOOD, GOOD, None, 0, None,
+             None) == 3                                  # H not a multiple of 8
+    g = lib.moe_combine_capped
+    g.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, P, P, P, P]
+    assert g(GOOD, GOOD, GOOD, None, 8, 4, 2, 0, 64, None, GOOD, None, None) == 1
+    assert g(GOOD, GOOD, GOOD, GOOD, 8, 4, 2, 0, 64, ODD, GOOD, None, None) == 3
+
+
 def test_combine_argument_checks(lib):
     f = lib.moe_combine
     f.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]
