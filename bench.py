@@ -400,13 +400,16 @@ def e2e_measure(layer, shape, T, inp, K, W, flush):
 
 
 def other_rows(dev, K, W, flush, peaks):
-    """The int8 weight-only layer (OLMoE shapes, T=64, uniform routing) and
-    the 16-layer OLMoE-shaped stack (skewed routing, T=64 and T=2048), each
+    """The int8 weight-only layer (OLMoE shapes, T=64, uniform routing), the
+    capacity-limited (token-dropping) layer at the pages' 4x load skew
+    (T=2048, dropless / CF 2.0 / CF 1.0) and the 16-layer OLMoE-shaped stack
+    (skewed routing, T=64 and T=2048), each
     captured in one CUDA graph and timed like the main workload: W warm-up
     steps, then K (capped for the long stack steps) timed steps with L2
     flushed before each.  Rooflines: weight bytes of the served groups at
     HBM bandwidth vs FLOPs at the bf16 peak (sustained for the stack, whose
     steps run for milliseconds), per layer, summed over the stack."""
+    import numpy as np
     import torch
 
     from grouped_expert_gemm_moe_gb300 import binding as B
@@ -435,6 +438,35 @@ def other_rows(dev, K, W, flush, peaks):
         "ffn": kind, "groups": ng, "algorithmic_bytes": bytes_, "bound": "hbm",
         "t_roof_us": round(t_roof, 2), "roofline_frac": round(t_roof / (ms * 1e3), 4)}
     del layer, cap, inp, q_gu, q_down
+    torch.cuda.empty_cache()
+
+    # token dropping at the pages' load skew (busiest expert ~4x the mean),
+    # OLMoE layer, T=2048: dropless vs capacity factors 2.0 and 1.0
+    sh = WL.OLMOE
+    T = 2048
+    inp = WL.make_layer(sh, T, "skew4", seed=0, device=dev)
+    for cf in (None, 2.0, 1.0):
+        layer = MoELayer(sh.H, sh.E, sh.k, sh.I, 0, False, w_gu=inp.w_gu, w_down=inp.w_down,
+                         device=dev, capacity_factor=cf)
+        cap = layer.capture(inp.x, inp.logits, ffn="gemm")
+        K2 = max(3, min(K, 200))
+        ms = statistics.fmean(time_graph(cap, K2, W, flush))
+        layer.check()
+        b = layer.buffers(T)
+        off = b.offsets.cpu().numpy()
+        served = int(off[sh.E])
+        ng = int(np.count_nonzero(np.diff(off[:sh.E + 1]) > 0))
+        H, I = sh.H, sh.I
+        bytes_ = ng * 3 * H * I * 2 + 2 * T * H * 2
+        flops = 6.0 * H * I * served
+        t_roof = max(bytes_ / bw, flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+        rows[f"capacity_{'dropless' if cf is None else f'cf{cf:g}'}_t2048_skew4"] = {
+            "us_per_layer": round(ms * 1e3, 2), "tokens_per_s": round(T / (ms / 1e3), 1),
+            "capacity": b.capacity, "dropped_slots": int(b.dropped.item()) if cf else 0,
+            "dropped_frac": round((T * sh.k - served) / (T * sh.k), 4), "steps": K2,
+            "t_roof_us": round(t_roof, 2), "roofline_frac": round(t_roof / (ms * 1e3), 4)}
+        del layer, cap
+    del inp
     torch.cuda.empty_cache()
 
     sh = WL.OLMOE_STACK
