@@ -49,6 +49,7 @@ _SIGS = {
     "moe_grouped_gemm_swiglu_w8": ([P, P, I, I, I, I, P, P, P, P, P, P, SZ, P, P], I),
     "moe_grouped_gemv_w8": ([P, P, I, I, I, I, P, P, P, P, P, P, SZ, P, P], I),
     "moe_combine": ([P, P, P, I, I, I, I, P, P, P, P], I),
+    "moe_router_route": ([P, P, P, I, I, I, I, I, P, P, P, P, P], I),
     "moe_grouped_gemm_gate_up": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_grouped_gemm_down": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_grouped_gemv_gate_up": ([P, P, I, I, I, I, P, P, P, P], I),
@@ -124,6 +125,23 @@ def moe_router_logits(x, w_r, bias, logits, stream=None):
         _dev(bias, "bias", torch.float32)
     _ok(_lib.moe_router_logits(_ptr(x), _ptr(w_r), _ptr(bias), T, H, E, _ptr(logits),
                                _stream(stream)), "moe_router_logits")
+
+
+def moe_router_route(x, w_r, bias, k, renormalize, topk_ids, topk_w, logits=None,
+                     dev_error=None, stream=None):
+    """Router logits + top-k in one launch (same ids and weights as
+    moe_router_logits followed by moe_route); logits: optional fp32 [T,E] output."""
+    T, H = x.shape
+    E = w_r.shape[0]
+    _dev(x, "x", torch.bfloat16); _dev(w_r, "w_r", torch.bfloat16)
+    _dev(topk_ids, "topk_ids", torch.int32); _dev(topk_w, "topk_w", torch.float32)
+    if logits is not None:
+        _dev(logits, "logits", torch.float32)
+    if bias is not None:
+        _dev(bias, "bias", torch.float32)
+    _ok(_lib.moe_router_route(_ptr(x), _ptr(w_r), _ptr(bias), T, H, E, k, int(renormalize),
+                              _ptr(logits), _ptr(topk_ids), _ptr(topk_w), _ptr(dev_error),
+                              _stream(stream)), "moe_router_route")
 
 
 def moe_route(logits, k, renormalize, topk_ids, topk_w, dev_error=None, stream=None):

@@ -19,7 +19,7 @@ namespace moe {
 // chosen expert and its weight.  Returns false (on every lane) if a logit is
 // NaN, leaving the outputs undefined.
 template <int PER_LANE>
-__device__ __forceinline__ bool route_token(const float *__restrict__ L, int E, int k,
+__device__ __forceinline__ bool route_token(const float *L, int E, int k,
                                             int renormalize, int &my_id, float &my_w) {
     const int lane = lane_id();
     float v[PER_LANE];
@@ -27,7 +27,7 @@ __device__ __forceinline__ bool route_token(const float *__restrict__ L, int E, 
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
         const int e = lane + 32 * i;
-        v[i] = e < E ? __ldg(L + e) : -INFINITY;
+        v[i] = e < E ? L[e] : -INFINITY;          // global or shared memory
         nan_seen |= isnan(v[i]);
     }
     if (__any_sync(FULL, nan_seen)) return false;

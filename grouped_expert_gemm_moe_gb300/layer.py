@@ -168,6 +168,18 @@ class MoELayer:
         self.combine(b, dst, residual, stream)
         return dst
 
+    def forward_routed(self, x, out=None, residual=None, ffn="auto", stream=None):
+        """The layer after routing: this batch's top-k ids and weights are
+        already in buffers(T) (e.g. from moe_router_route)."""
+        T = x.shape[0]
+        b = self.buffers(T)
+        kind = self.choose_ffn(T) if ffn == "auto" else ffn
+        self.permute(x, b, stream)
+        self.ffn(b, kind, stream)
+        dst = b.out if out is None else out
+        self.combine(b, dst, residual, stream)
+        return dst
+
     def capture(self, x: torch.Tensor, logits: torch.Tensor, out=None, residual=None,
                 ffn="auto") -> "CapturedForward":
         """Record one forward pass over the fixed device buffers x / logits
@@ -203,7 +215,8 @@ class CapturedForward:
 
 class MoEStack:
     """L MoE blocks with residual adds, x_{l+1} = bf16(x_l + MoE_l(x_l)); the
-    router logits of block l come from x_l on the device."""
+    routing of block l comes from x_l on the device, router logits and top-k
+    in one launch (moe_router_route)."""
 
     def __init__(self, layers: list[MoELayer], routers: list[torch.Tensor], bias=None):
         self.layers = layers
@@ -225,11 +238,14 @@ class MoEStack:
             pair = self._x[T] = (torch.empty_like(x), torch.empty_like(x))
         cur = x
         for i, (layer, w_r) in enumerate(zip(self.layers, self.routers)):
-            B.moe_router_logits(cur, w_r, self.bias, L, stream)
+            b = layer.buffers(T)
+            B.moe_router_route(cur, w_r, self.bias, layer.k, layer.renormalize, b.topk_ids,
+                               b.topk_w, logits=L if keep is not None else None,
+                               dev_error=layer.err, stream=stream)
             if keep is not None:
                 keep.append((cur.clone(), L.clone()))
             nxt = pair[i % 2]
-            layer.forward(cur, L, out=nxt, residual=cur, ffn=ffn, stream=stream)
+            layer.forward_routed(cur, out=nxt, residual=cur, ffn=ffn, stream=stream)
             cur = nxt
         return cur
 

@@ -88,6 +88,20 @@ moe_status moe_router_logits(const uint16_t *x, const uint16_t *w_r, const float
                              int H, int E, float *logits, cudaStream_t stream);
 
 /*
+ * moe_router_route -- moe_router_logits and moe_route in one launch: a CTA
+ * forms its tokens' logits in shared memory (the same fixed summation order
+ * as moe_router_logits, so the same fp32 values) and routes them there, so
+ * topk_ids / topk_w equal those of the two calls bit for bit, and the
+ * logits make no round trip through global memory.  logits: [T,E] fp32
+ * output or NULL (not written).  Other arguments as for the two calls;
+ * E <= 1024, 1 <= k <= min(E, 32).
+ */
+moe_status moe_router_route(const uint16_t *x, const uint16_t *w_r, const float *bias, int T,
+                            int H, int E, int k, int renormalize, float *logits,
+                            int32_t *topk_ids, float *topk_w, int32_t *dev_error,
+                            cudaStream_t stream);
+
+/*
  * moe_route -- top-k routing, one warp per token ("switchyard" page, "Route
  * and sort": each token routed in one warp).
  * logits: [T,E] fp32.  topk_ids: [T,k] int32, the k experts with the

@@ -368,3 +368,36 @@ def test_gemm_tile_shapes_agree(B, L, tile):
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("T,E,k,renorm", [(1, 64, 8, 0), (64, 64, 8, 0), (700, 96, 6, 1),
+                                          (2048, 64, 6, 0), (37, 256, 4, 1)])
+def test_fused_router_route_matches_the_two_calls(B, T, E, k, renorm):
+    """moe_router_route: logits, ids and weights bit-identical to
+    moe_router_logits followed by moe_route; logits vs the oracle (fp64)."""
+    H = 2048
+    g = torch.Generator().manual_seed(T + E)
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16).to(DEV)
+    w_r = (torch.randn((E, H), generator=g) * 0.02).to(torch.bfloat16).to(DEV)
+    bias = W.zipf_bias(E, 1.2).to(DEV) if E == 64 else None
+    L1 = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    ids1 = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w1 = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    err = B.new_error_word(DEV)
+    B.moe_router_logits(x, w_r, bias, L1)
+    B.moe_route(L1, k, renorm, ids1, w1, err)
+    L2 = torch.empty_like(L1)
+    ids2, w2 = torch.empty_like(ids1), torch.empty_like(w1)
+    B.moe_router_route(x, w_r, bias, k, renorm, ids2, w2, logits=L2, dev_error=err)
+    ids3, w3 = torch.empty_like(ids1), torch.empty_like(w1)
+    B.moe_router_route(x, w_r, bias, k, renorm, ids3, w3, dev_error=err)   # no logits out
+    B.check_device_error(err, "router_route")
+    assert torch.equal(L1, L2)
+    assert torch.equal(ids1, ids2) and torch.equal(ids1, ids3)
+    assert torch.equal(w1.view(torch.int32), w2.view(torch.int32))
+    assert torch.equal(w1.view(torch.int32), w3.view(torch.int32))
+    tok = sample_tokens(T, n=16)
+    ref = oracle.router_logits(W.bf16_bits(x.cpu())[tok], W.bf16_bits(w_r.cpu()),
+                               None if bias is None else bias.cpu().numpy())
+    assert np.abs(L2.cpu().numpy()[tok] - ref).max() <= 1e-4 * np.abs(ref).max()
+
