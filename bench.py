@@ -249,10 +249,13 @@ class Phases:
         e.record()
 
 
-def kernels_per_step(layer, T):
-    """Kernels of one layer step: route + permute (1 fused launch for small
-    batches; else the routing kernel plus 1 permute kernel up to 1024 slots
-    or 3 above), then gate/up, down and combine."""
+def kernels_per_step(layer, T, kind="auto"):
+    """Kernels of one layer step: the single-launch decode layer is 1;
+    otherwise route + permute (1 fused launch for small batches; else the
+    routing kernel plus 1 permute kernel up to 1024 slots or 3 above), then
+    gate/up, down and combine."""
+    if kind == "decode":
+        return 1
     if layer.fused_route_permute_ok(T):
         rp = 1
     else:
@@ -347,18 +350,41 @@ def measure_T(layer, shape, T, x, logits, K, W, flush, peaks, workload):
     """Layer time from K steps of the whole forward pass captured in one
     CUDA graph; the gate/up kernel's time from K further steps recorded as
     three graphs with events around the gate/up launch."""
-    kind = layer.choose_ffn(T)
+    kind = layer.choose_path(T, x.dtype)
     cap = layer.capture(x, logits, ffn=kind)
     step = time_graph(cap, K, W, flush)
+    ms = statistics.fmean(step)
+    if kind == "decode":
+        # one kernel is the whole layer: its roofline is the layer's
+        b = layer.buffers(T)
+        layer.route(logits, b)
+        layer.permute(x, b)
+        n_groups = touched_groups(layer, b)
+        roof = layer_roofline(shape, T, n_groups, peaks)
+        return dict(kind=kind, step_ms=step, gate_up_ms=ms, ms=ms, n_groups=n_groups, roof=roof,
+                    kroof=decode_kernel_roofline(shape, T, n_groups, ms, peaks, workload))
     ph = Phases(layer, x, logits, kind)
     _, gu = time_steps(ph, K, W, flush)
     n_groups = touched_groups(layer, ph.b)
-    ms = statistics.fmean(step)
     roof = layer_roofline(shape, T, n_groups, peaks)
     return dict(kind=kind, step_ms=step, gate_up_ms=statistics.fmean(gu), ms=ms,
                 n_groups=n_groups, roof=roof,
                 kroof=kernel_roofline(shape, T, n_groups, statistics.fmean(gu), peaks, kind,
                                       workload))
+
+
+def decode_kernel_roofline(shape, T, n_groups, step_ms, peaks, workload):
+    """Roofline of the single-launch decode layer: its algorithmic bytes are
+    all weights of the served groups (3*H*I*2 each) plus x in and out; the
+    step time is the kernel's (plus a 4-byte memset node)."""
+    H, I = shape.H, shape.I
+    bytes_ = n_groups * 3 * H * I * 2 + 2 * T * H * 2
+    ach = bytes_ / (step_ms / 1e3) / 1e9
+    return {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": round(ach, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+            "traffic": profiled_traffic("decode_layer_kernel", workload),
+            "algorithmic_bytes": bytes_, "avg_launch_us": round(step_ms * 1e3, 2),
+            "peak_source": f"{peaks['source']} (STREAM copy, burst)"}
 
 
 def e2e_measure(layer, shape, T, inp, K, W, flush):
@@ -642,7 +668,8 @@ def run_ours(args):
                     "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": round(e2e_ms * 1e3, 2),
                     "path": "pinned host x+logits -> MoELayer captured forward -> pinned host out"},
-            "gpu_launches": 2 * kernels_per_step(layer, T) * args.steps,   # both timed passes
+            "gpu_launches": (1 if m["kind"] == "decode" else 2) * kernels_per_step(
+                layer, T, m["kind"]) * args.steps,           # every timed pass
             "clocks": clocks,
         }
         if base is not None:

@@ -50,6 +50,8 @@ _SIGS = {
     "moe_grouped_gemv_w8": ([P, P, I, I, I, I, P, P, P, P, P, P, SZ, P, P], I),
     "moe_combine": ([P, P, P, I, I, I, I, P, P, P, P], I),
     "moe_router_route": ([P, P, P, I, I, I, I, I, P, P, P, P, P], I),
+    "moe_decode_workspace_size": ([I, I, I, I, I, I], SZ),
+    "moe_decode_layer": ([P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P, P], I),
     "moe_grouped_gemm_gate_up": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_grouped_gemm_down": ([P, P, I, I, I, I, P, P, P, P], I),
     "moe_grouped_gemv_gate_up": ([P, P, I, I, I, I, P, P, P, P], I),
@@ -371,6 +373,38 @@ def moe_combine_capped(y_perm, row_of_slot, topk_w, offsets, E, S, out, residual
     _ok(_lib.moe_combine_capped(_ptr(y_perm), _ptr(row_of_slot), _ptr(topk_w), _ptr(offsets), E,
                                 T, k, S, H, _ptr(residual), _ptr(out), _ptr(dev_error),
                                 _stream(stream)), "moe_combine_capped")
+
+
+DECODE_LAYER_MAX_T = 8
+DECODE_LAYER_MAX_SLOTS = 64
+DECODE_LAYER_MAX_E = 256
+
+
+def moe_decode_workspace_size(T, E, S, k, H, I) -> int:
+    return int(_lib.moe_decode_workspace_size(T, E, S, k, H, I))
+
+
+def moe_decode_layer(logits, x, k, renormalize, S, w_gu, w_down, out, workspace, residual=None,
+                     topk_ids=None, topk_w=None, dev_error=None, stream=None):
+    """The whole layer for T <= 8 tokens in one cooperative launch (route,
+    grouped GEMV gate/up + down, combine); same bytes as the separate calls."""
+    _dev(logits, "logits", torch.float32); _dev(x, "x", torch.bfloat16)
+    _dev(w_gu, "w_gu", torch.bfloat16); _dev(w_down, "w_down", torch.bfloat16)
+    _dev(out, "out", torch.bfloat16); _dev(workspace, "workspace")
+    if residual is not None:
+        _dev(residual, "residual", torch.bfloat16)
+    if topk_ids is not None:
+        _dev(topk_ids, "topk_ids", torch.int32)
+    if topk_w is not None:
+        _dev(topk_w, "topk_w", torch.float32)
+    T, E = logits.shape
+    H = x.shape[1]
+    I = w_down.shape[2]
+    wsb = workspace.numel() * workspace.element_size()
+    _ok(_lib.moe_decode_layer(_ptr(logits), _ptr(x), T, E, S, k, int(renormalize), H, I,
+                              _ptr(w_gu), _ptr(w_down), _ptr(residual), _ptr(out),
+                              _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), wsb,
+                              _ptr(dev_error), _stream(stream)), "moe_decode_layer")
 
 
 def moe_quantize_w8(w: torch.Tensor):

@@ -128,6 +128,15 @@ __device__ __forceinline__ uint4 ld_stream(const void *p, uint64_t policy) {
                  : "l"(p), "l"(policy));
     return r;
 }
+// coherent at GPU scope (L2, not L1): for data other CTAs of the same
+// launch wrote before a grid-wide barrier
+__device__ __forceinline__ uint4 ld_cg(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
 __device__ __forceinline__ uint4 ld_nc(const void *p) {       // read-only, cached
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }

@@ -19,7 +19,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "common.cuh"
+#include "gemv_tasks.cuh"
 
 namespace moe {
 
@@ -67,15 +67,6 @@ __device__ __forceinline__ int load_active_groups(ActiveGroups &ag, const int32_
     return ag.count;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
-
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x);
-    f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
-    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z);
-    f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
-}
-
 // 16 int8 (biased) -> 16 fp32
 __device__ __forceinline__ void unpack16_s8(const uint4 v, float (&f)[16]) {
     const uint32_t w[4] = {bias_s8x4(v.x), bias_s8x4(v.y), bias_s8x4(v.z), bias_s8x4(v.w)};
@@ -114,41 +105,11 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_gateup_bf16(
         for (int rb = 0; rb < nr; rb += NR) {
             const int nrr = min(NR, nr - rb);
             const uint16_t *xr = x_perm + static_cast<int64_t>(r0 + rb) * H;
+            const uint16_t *xrow[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) xrow[r] = xr + static_cast<int64_t>(r) * H;
             float sg[NR], su[NR];
-#pragma unroll
-            for (int r = 0; r < NR; ++r) sg[r] = su[r] = 0.f;
-            for (int seg = 0; seg < chunks; seg += 32 * NCH) {
-                uint4 vg[NCH], vu[NCH], vx[NR][NCH];
-#pragma unroll
-                for (int u = 0; u < NCH; ++u) {
-                    const int q = seg + lane + 32 * u;
-                    if (q < chunks) {
-                        vg[u] = ld_stream(wg + q * 8, pol);
-                        vu[u] = ld_stream(wu + q * 8, pol);
-#pragma unroll
-                        for (int r = 0; r < NR; ++r)
-                            if (r < nrr) vx[r][u] = ld_nc(xr + static_cast<int64_t>(r) * H + q * 8);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < NCH; ++u) {
-                    if (seg + lane + 32 * u >= chunks) continue;
-                    float fg[8], fu[8];
-                    unpack8(vg[u], fg);
-                    unpack8(vu[u], fu);
-#pragma unroll
-                    for (int r = 0; r < NR; ++r) {
-                        if (r >= nrr) break;
-                        float fx[8];
-                        unpack8(vx[r][u], fx);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            sg[r] = fmaf(fg[e], fx[e], sg[r]);
-                            su[r] = fmaf(fu[e], fx[e], su[r]);
-                        }
-                    }
-                }
-            }
+            gateup_partial_bf16<NCH, NR>(xrow, nrr, wg, wu, chunks, pol, sg, su);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 if (r >= nrr) break;
@@ -186,43 +147,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_down_bf16(
             const int nrr = min(NR, nr - rb);
             const uint16_t *hr = h + static_cast<int64_t>(r0 + rb) * I;
             float acc[NR][RW];
-#pragma unroll
-            for (int r = 0; r < NR; ++r)
-#pragma unroll
-                for (int w = 0; w < RW; ++w) acc[r][w] = 0.f;
-            for (int seg = 0; seg < chunks; seg += 32 * NCH) {
-                uint4 vw[RW][NCH], vx[NR][NCH];
-#pragma unroll
-                for (int u = 0; u < NCH; ++u) {
-                    const int q = seg + lane + 32 * u;
-                    if (q < chunks) {
-#pragma unroll
-                        for (int w = 0; w < RW; ++w)
-                            if (n0 + w < H) vw[w][u] = ld_stream(wd + static_cast<int64_t>(w) * I + q * 8, pol);
-#pragma unroll
-                        for (int r = 0; r < NR; ++r)
-                            if (r < nrr) vx[r][u] = ld_nc(hr + static_cast<int64_t>(r) * I + q * 8);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < NCH; ++u) {
-                    if (seg + lane + 32 * u >= chunks) continue;
-#pragma unroll
-                    for (int r = 0; r < NR; ++r) {
-                        if (r >= nrr) break;
-                        float fx[8];
-                        unpack8(vx[r][u], fx);
-#pragma unroll
-                        for (int w = 0; w < RW; ++w) {
-                            if (n0 + w >= H) break;
-                            float fw[8];
-                            unpack8(vw[w][u], fw);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[r][w] = fmaf(fw[e], fx[e], acc[r][w]);
-                        }
-                    }
-                }
-            }
+            down_partial_bf16<NCH, RW, NR>(hr, I, nrr, wd, n0, H, chunks, pol, acc);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 if (r >= nrr) break;

@@ -18,6 +18,11 @@ from . import binding as B
 # used instead of the tensor-core grouped GEMM.
 GEMV_MAX_ROWS_PER_GROUP = 0.25
 
+# Largest batch for which "auto" takes the single-launch decode layer
+# (measured on GB300: faster than the separate calls at T = 1 and 2, the
+# tensor-core GEMM is faster from T = 4 on).
+DECODE_LAYER_AUTO_MAX_T = 2
+
 
 @dataclass
 class LayerBuffers:
@@ -64,6 +69,7 @@ class MoELayer:
             self.w_gu, self.w_down = w_gu, w_down
         self.err = B.new_error_word(self.device)
         self._bufs: dict[int, LayerBuffers] = {}
+        self._decode_ws: dict[int, torch.Tensor] = {}
 
     def rows(self, T: int) -> int:
         return T * self.k + self.S * T
@@ -93,6 +99,19 @@ class MoELayer:
             )
             self._bufs[T] = b
         return b
+
+    def decode_layer_ok(self, T: int, x_dtype=torch.bfloat16) -> bool:
+        """The single-launch decode layer applies: bf16 experts and
+        activations, dropless, T <= 8, T*k <= 64, S*T <= 64, E <= 256."""
+        return (not self.int8 and self.capacity_factor is None and x_dtype == torch.bfloat16
+                and T <= B.DECODE_LAYER_MAX_T and T * self.k <= B.DECODE_LAYER_MAX_SLOTS
+                and self.S * T <= 64 and self.S <= 32 and self.E <= B.DECODE_LAYER_MAX_E)
+
+    def choose_path(self, T: int, x_dtype=torch.bfloat16) -> str:
+        """What forward(ffn="auto") runs: "decode", "gemv" or "gemm"."""
+        if T <= DECODE_LAYER_AUTO_MAX_T and self.decode_layer_ok(T, x_dtype):
+            return "decode"
+        return self.choose_ffn(T)
 
     def choose_ffn(self, T: int) -> str:
         return "gemv" if self.rows(T) / self.G <= GEMV_MAX_ROWS_PER_GROUP else "gemm"
@@ -157,11 +176,29 @@ class MoELayer:
             return
         B.moe_combine(b.y_perm, b.row_of_slot, b.topk_w, self.S, out, residual, self.err, stream)
 
+    def decode_workspace(self, T: int) -> torch.Tensor:
+        ws = self._decode_ws.get(T)
+        if ws is None:
+            n = B.moe_decode_workspace_size(T, self.E, self.S, self.k, self.H, self.I)
+            ws = self._decode_ws[T] = torch.empty(n, dtype=torch.uint8, device=self.device)
+        return ws
+
     def forward(self, x, logits, out=None, residual=None, ffn="auto", stream=None):
-        """out[t] = sum_j w[t,j] FFN_{id[t,j]}(x[t]) + sum_s FFN_{E+s}(x[t]) (+ residual[t])."""
+        """out[t] = sum_j w[t,j] FFN_{id[t,j]}(x[t]) + sum_s FFN_{E+s}(x[t]) (+ residual[t]).
+        ffn: "gemm", "gemv", "decode" (the single-launch decode layer) or
+        "auto" (decode where it applies and measured fastest, else by rows
+        per group)."""
         T = x.shape[0]
         b = self.buffers(T)
-        kind = self.choose_ffn(T) if ffn == "auto" else ffn
+        kind = self.choose_path(T, x.dtype) if ffn == "auto" else ffn
+        if kind == "decode":
+            if not self.decode_layer_ok(T, x.dtype):
+                raise ValueError("the single-launch decode layer does not apply to this batch")
+            dst = b.out if out is None else out
+            B.moe_decode_layer(logits, x, self.k, self.renormalize, self.S, self.w_gu,
+                               self.w_down, dst, self.decode_workspace(T), residual, b.topk_ids,
+                               b.topk_w, self.err, stream)
+            return dst
         self.route_permute(logits, x, b, stream)
         self.ffn(b, kind, stream)
         dst = b.out if out is None else out
