@@ -541,12 +541,13 @@ def oracle_sample(inp, tokens):
     return dict(logits=np.ascontiguousarray(logits), x=np.ascontiguousarray(x))
 
 
-def run_oracle_tokens(inp, host, tokens, wbits):
+def run_oracle_tokens(inp, host, tokens, wbits, nthreads=0):
     import oracle
     sh = inp.shape
     ids, w = oracle.route(host["logits"], sh.k, sh.renormalize)
     oracle.permute(ids, sh.E, sh.S)
-    return oracle.moe_layer(host["x"], ids, w, sh.E, sh.S, wbits[0], wbits[1])
+    return oracle.moe_layer(host["x"], ids, w, sh.E, sh.S, wbits[0], wbits[1],
+                            nthreads=nthreads)
 
 
 def cpu_baseline(inp, gpu_out, max_tokens=64):
@@ -568,9 +569,17 @@ def cpu_baseline(inp, gpu_out, max_tokens=64):
     rel = float(np.linalg.norm(got - y) / np.linalg.norm(y))
     mx = float(np.abs(got - y).max() / np.abs(y).max())
     cores = min(len(tokens), oracle.num_threads())
+    # the same oracle on one thread, for scale (a smaller sample)
+    t1 = tokens[:min(len(tokens), 4)]
+    h1 = oracle_sample(inp, t1)
+    t0 = time.perf_counter()
+    run_oracle_tokens(inp, h1, t1, wbits, nthreads=1)
+    sec1 = time.perf_counter() - t0
     return dict(value=round(len(tokens) / sec, 3), unit=UNIT, cores=cores, kind="oracle",
                 sample=f"route+permute+layer of tokens 0..{len(tokens) - 1} of the timed batch "
                        f"({len(tokens)} tokens, {sec:.2f} s)",
+                value_1_thread=round(len(t1) / sec1, 3),
+                sample_1_thread=f"tokens 0..{len(t1) - 1} on one thread ({sec1:.2f} s)",
                 parity={"rel_frobenius": rel, "max_rel": mx, "ok": rel <= 5e-3 and mx <= 2e-2})
 
 
@@ -674,7 +683,8 @@ def run_ours(args):
         }
         if base is not None:
             line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind",
-                                                         "sample")}
+                                                         "sample", "value_1_thread",
+                                                         "sample_1_thread")}
             line["parity_vs_oracle"] = base["parity"]
         print(json.dumps(line), flush=True)
     if world > 1:

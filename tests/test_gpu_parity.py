@@ -401,3 +401,40 @@ def test_fused_router_route_matches_the_two_calls(B, T, E, k, renorm):
                                None if bias is None else bias.cpu().numpy())
     assert np.abs(L2.cpu().numpy()[tok] - ref).max() <= 1e-4 * np.abs(ref).max()
 
+
+
+@pytest.mark.parametrize("ffn", ["gemm", "gemv"])
+@pytest.mark.parametrize("T", [16, 40])
+def test_maximum_groups_and_k(B, L, ffn, T):
+    """The limits: G = E + S = 1024 groups (1000 routed, 24 shared) and k = 32;
+    T=16 uses the one-launch permute (512 slots), T=40 the chunked one."""
+    sh = W.MoEShape("max", H=256, E=1000, k=32, I=128, S=24)
+    inp = W.make_layer(sh, T, "uniform", seed=8)
+    h = host_inputs(inp)
+    layer = make_layer_obj(L, inp)
+    out = layer.forward(inp.x.to(DEV), inp.logits.to(DEV), ffn=ffn)
+    layer.check()
+    b = layer.buffers(T)
+    ids, w, y = oracle_out(inp, h)
+    np.testing.assert_array_equal(b.topk_ids.cpu().numpy(), ids)
+    np.testing.assert_array_equal(b.offsets.cpu().numpy(), oracle.permute(ids, sh.E, sh.S)[0])
+    assert_close(to_np(out), y, f"G=1024 k=32 T={T} {ffn}")
+
+
+def test_deepseek_16384_tokens(B, L):
+    """A batch 8x the largest configured one (131072 permuted rows, 128
+    permute chunks), checked on sampled tokens."""
+    sh = W.DEEPSEEK
+    T = 16384
+    inp = W.make_layer(sh, T, "zipf", seed=2, device=DEV)
+    layer = make_layer_obj(L, inp)
+    out = layer.forward(inp.x, inp.logits, ffn="gemm")
+    layer.check()
+    tok = sample_tokens(T, n=24)
+    h = host_inputs(inp)
+    ids, w = oracle.route(h["logits"], sh.k, sh.renormalize)
+    np.testing.assert_array_equal(layer.buffers(T).topk_ids.cpu().numpy(), ids)
+    np.testing.assert_array_equal(layer.buffers(T).offsets.cpu().numpy(),
+                                  oracle.permute(ids, sh.E, sh.S)[0])
+    y = oracle.moe_layer(h["x"], ids, w, sh.E, sh.S, h["w_gu"], h["w_down"], tokens=tok)
+    assert_close(to_np(out)[tok], y, "DeepSeek T=16384")
