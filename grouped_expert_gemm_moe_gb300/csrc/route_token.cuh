@@ -6,7 +6,8 @@
 // descending order ("switchyard" page, 02 Kernels and dispatch, "Route and
 // sort": each token routed in one warp).  The softmax runs over all E
 // logits; L_e - max is corrected for its fp32 rounding and the denominator is
-// summed in fp64, so each weight is within a few fp32 ulps of the exact value.
+// summed in fp32 with compensation, so each weight is within a few fp32 ulps
+// of the exact value.
 #pragma once
 
 #include <math.h>
@@ -73,20 +74,39 @@ __device__ __forceinline__ bool route_token(const float *L, int E, int k,
         const float e = expf(s);
         return fmaf(e, r, e);
     };
-    double den = 0.0;
+    // sums of positive terms in fp32 with their rounding errors carried
+    // alongside (Knuth's two-sum), so each sum is within ~1 ulp of exact
+    // without double-precision arithmetic (slow on this part)
+    auto add2 = [](float &hi, float &lo, float x) {
+        const float s = hi + x;
+        const float bb = s - hi;
+        lo += (hi - (s - bb)) + (x - bb);
+        hi = s;
+    };
+    float den = 0.f, den_lo = 0.f;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) den += static_cast<double>(shifted_exp(v[i]));
+        if (e < E) add2(den, den_lo, shifted_exp(v[i]));
     }
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(FULL, den, d);
+    for (int d = 16; d > 0; d >>= 1) {
+        const float oh = __shfl_xor_sync(FULL, den, d), ol = __shfl_xor_sync(FULL, den_lo, d);
+        add2(den, den_lo, oh);
+        den_lo += ol;
+    }
+    den += den_lo;
 
     const float ej = lane < k ? shifted_exp(my_val) : 0.f;
-    double sel = static_cast<double>(ej);
+    float sel = ej, sel_lo = 0.f;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) sel += __shfl_xor_sync(FULL, sel, d);
-    my_w = static_cast<float>(static_cast<double>(ej) / (renormalize ? sel : den));
+    for (int d = 16; d > 0; d >>= 1) {
+        const float oh = __shfl_xor_sync(FULL, sel, d), ol = __shfl_xor_sync(FULL, sel_lo, d);
+        add2(sel, sel_lo, oh);
+        sel_lo += ol;
+    }
+    sel += sel_lo;
+    my_w = __fdiv_rn(ej, renormalize ? sel : den);
     return true;
 }
 
