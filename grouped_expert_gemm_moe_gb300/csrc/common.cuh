@@ -208,6 +208,17 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// 3-D tiled TMA load global -> shared (box [z][y][x], x innermost).
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y, uint64_t policy) {

@@ -10,9 +10,11 @@
 //    (one HBM read, the rest L2 hits).  The tile table is built on the
 //    device from the offsets table: the host never learns the group sizes;
 //  * warp 0: TMA producer (one thread) filling a ring of STAGES shared
-//    memory stages: the activation tile (token rows, K-major, 128-byte
-//    swizzle, fetched as 16-row boxes so a small group only pulls the rows
-//    it has) and the weight tile;
+//    memory stages with two copies each: the activation tile (token rows,
+//    K-major, 128-byte swizzle, one box of 16/32/64/128 rows, the smallest
+//    that holds the tile's rows) and the weight tile (SwiGLU: the gate rows
+//    and the matching up rows in one 3-D box).  Copies per stage are the
+//    ring's cost here, not bytes: on GB300 a third copy per stage cost 4-6 %;
 //  * warp 1: TMEM allocator and MMA issuer (one thread): tcgen05.mma
 //    kind::f16, M = 128 token rows, N = BN weight rows, K = 16 per
 //    instruction, fp32 accumulators in TMEM, double-buffered (2 x BN
@@ -51,7 +53,9 @@ struct TcCfg {
 // PLAIN : out = y [M, NOUT=H], weights [G*H,  K=I].
 template <bool SWIGLU, int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_act,
+    tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_act16,
+                    const __grid_constant__ CUtensorMap tm_act32,
+                    const __grid_constant__ CUtensorMap tm_act64,
                     const __grid_constant__ CUtensorMap tm_act128,
                     const __grid_constant__ CUtensorMap tm_w, const int32_t *__restrict__ offsets,
                     int G, int M, int K, int R, int NOUT, int UP_OFF, uint16_t *__restrict__ out,
@@ -90,7 +94,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_act16);
+        prefetch_tmap(&tm_act32);
+        prefetch_tmap(&tm_act64);
         prefetch_tmap(&tm_act128);
         prefetch_tmap(&tm_w);
     }
@@ -115,12 +121,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile(t, s_tile, s_off, G);
-                // a tile with more than 64 rows takes one 128-row box; a smaller
-                // one only the 16-row boxes it needs (rows past the group are
-                // loaded but never stored)
-                const bool full_box = ti.nrows > 64;
-                const int nbox = full_box ? TC_BM / TC_ABOX : (ti.nrows + TC_ABOX - 1) / TC_ABOX;
-                const uint32_t bytes = nbox * TC_ABOX * TC_BK * 2 + C::B_BYTES;
+                // the token rows as one box of 16, 32, 64 or 128 rows, the
+                // smallest that holds the tile's rows (one copy per stage; rows
+                // past the group are loaded but never stored)
+                const int abox = ti.nrows <= 16 ? 16 : ti.nrows <= 32 ? 32
+                                                     : ti.nrows <= 64 ? 64 : 128;
+                const CUtensorMap *tm_a = abox == 16 ? &tm_act16 : abox == 32 ? &tm_act32
+                                        : abox == 64 ? &tm_act64 : &tm_act128;
+                const uint32_t bytes = abox * TC_BK * 2 + C::B_BYTES;
                 const int wrow = ti.g * R + ti.nt * n_per_tile;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, dev_error)) {
@@ -131,15 +139,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     uint8_t *a = sA + stage * C::A_BYTES;
                     uint8_t *b = sB + stage * C::B_BYTES;
                     const int kx = kb * TC_BK;
-                    if (full_box)
-                        tma_load_2d(a, &tm_act128, &full[stage], kx, ti.m0, pol_a);
-                    else
-                        for (int bx = 0; bx < nbox; ++bx)
-                            tma_load_2d(a + bx * TC_ABOX * 128, &tm_act, &full[stage], kx,
-                                        ti.m0 + bx * TC_ABOX, pol_a);
-                    if (SWIGLU) {
-                        tma_load_2d(b, &tm_w, &full[stage], kx, wrow, pol_w);
-                        tma_load_2d(b + (BN / 2) * 128, &tm_w, &full[stage], kx, wrow + UP_OFF,
+                    tma_load_2d(a, tm_a, &full[stage], kx, ti.m0, pol_a);
+                    if (SWIGLU) {          // gate rows and up rows in one 3-D copy
+                        tma_load_3d(b, &tm_w, &full[stage], kx, ti.nt * n_per_tile, 2 * ti.g,
                                     pol_w);
                     } else {
                         tma_load_2d(b, &tm_w, &full[stage], kx, wrow, pol_w);
@@ -275,18 +277,19 @@ template <bool SWIGLU, int BN>
 static moe_status launch_tc(const void *act, const void *w, const int32_t *offsets, int G, int M,
                             int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
                             cudaStream_t stream) {
-    CUtensorMap tm_act, tm_w;
-    CUtensorMap tm_act128;
-    if (!encode_bf16_2d(&tm_act, act, K, M, TC_ABOX)) return MOE_ERR_CUDA;
-    if (!encode_bf16_2d(&tm_act128, act, K, M, TC_BM)) return MOE_ERR_CUDA;
-    if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, SWIGLU ? BN / 2 : BN))
+    CUtensorMap tm_act16, tm_act32, tm_act64, tm_act128, tm_w;
+    if (!encode_bf16_2d(&tm_act16, act, K, M, 16) || !encode_bf16_2d(&tm_act32, act, K, M, 32) ||
+        !encode_bf16_2d(&tm_act64, act, K, M, 64) || !encode_bf16_2d(&tm_act128, act, K, M, TC_BM))
+        return MOE_ERR_CUDA;
+    if (SWIGLU ? !encode_gate_up_3d(&tm_w, w, K, UP_OFF, G, BN / 2)
+               : !encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, BN))
         return MOE_ERR_CUDA;
     const size_t smem = TcCfg<BN>::smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
     static int attr_done[64] = {0};
     if (!raise_smem_limit(tc_grouped_gemm<SWIGLU, BN>, attr_done)) return MOE_ERR_CUDA;
-    launch(tc_grouped_gemm<SWIGLU, BN>, sm_count(), TC_THREADS, smem, stream, 
-        tm_act, tm_act128, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
+    launch(tc_grouped_gemm<SWIGLU, BN>, sm_count(), TC_THREADS, smem, stream, tm_act16, tm_act32,
+           tm_act64, tm_act128, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
 }
 

@@ -66,26 +66,6 @@ __device__ __forceinline__ PTile p_decode(int t, const int *s_tile, const int *s
     return ti;
 }
 
-// TMA loads of one 128-row half of a token block: one 128-row box when the
-// half has more than 64 rows, else the 16-row boxes it needs.
-__device__ __forceinline__ uint32_t half_bytes(int rows) {
-    if (rows <= 0) return 0;
-    if (rows > 64) return TC_BM * 128;
-    return static_cast<uint32_t>((rows + TC_ABOX - 1) / TC_ABOX) * TC_ABOX * 128;
-}
-__device__ __forceinline__ void load_half(uint8_t *dst, const CUtensorMap *tm16,
-                                          const CUtensorMap *tm128, uint64_t *bar, int kx,
-                                          int m0, int rows, uint64_t pol) {
-    if (rows <= 0) return;
-    if (rows > 64) {
-        tma_load_2d(dst, tm128, bar, kx, m0, pol);
-    } else {
-        const int nbox = (rows + TC_ABOX - 1) / TC_ABOX;
-        for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(dst + bx * TC_ABOX * 128, tm16, bar, kx, m0 + bx * TC_ABOX, pol);
-    }
-}
-
 // SWIGLU: out = h [M, NOUT=I], weights [G*2I, K=H], up rows at +UP_OFF = I.
 // PLAIN : out = y [M, NOUT=H], weights [G*H,  K=I].
 template <bool SWIGLU>
@@ -93,6 +73,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     tc_grouped_gemm_256(const __grid_constant__ CUtensorMap tm_act,
                         const __grid_constant__ CUtensorMap tm_act128,
                         const __grid_constant__ CUtensorMap tm_w,
+                        const __grid_constant__ CUtensorMap tm_act32,
+                        const __grid_constant__ CUtensorMap tm_act64,
+                        const __grid_constant__ CUtensorMap tm_act256,
                         const int32_t *__restrict__ offsets, int G, int M, int K, int R,
                         int NOUT, int UP_OFF, uint16_t *__restrict__ out, int32_t *dev_error) {
     using C = PCfg;
@@ -127,7 +110,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_act32);
+        prefetch_tmap(&tm_act64);
         prefetch_tmap(&tm_act128);
+        prefetch_tmap(&tm_act256);
         prefetch_tmap(&tm_w);
     }
     if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
@@ -150,9 +136,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const PTile ti = p_decode(t, s_tile, s_off, G);
-                const int rows1 = min(TC_BM, ti.rows);
-                const int rows2 = ti.rows - rows1;
-                const uint32_t bytes = half_bytes(rows1) + half_bytes(rows2) + C::B_BYTES;
+                // the block's token rows as one box of 16 .. 256 rows (the two
+                // 128-row halves are contiguous in the stage), the smallest
+                // that holds them; rows past the group are loaded, never stored
+                const int abox = ti.rows <= 16 ? 16 : ti.rows <= 32 ? 32 : ti.rows <= 64 ? 64
+                                 : ti.rows <= 128 ? 128 : 256;
+                const CUtensorMap *tm_a = abox == 16 ? &tm_act : abox == 32 ? &tm_act32
+                                        : abox == 64 ? &tm_act64 : abox == 128 ? &tm_act128
+                                                                              : &tm_act256;
+                const uint32_t bytes = abox * 128 + C::B_BYTES;
                 const int wrow = ti.g * R + ti.nt * n_per_tile;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, dev_error)) {
@@ -164,12 +156,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     uint8_t *a2 = a1 + C::A_BYTES;
                     uint8_t *b = a2 + C::A_BYTES;
                     const int kx = kb * TC_BK;
-                    load_half(a1, &tm_act, &tm_act128, &full[stage], kx, ti.m0, rows1, pol_a);
-                    load_half(a2, &tm_act, &tm_act128, &full[stage], kx, ti.m0 + TC_BM, rows2,
-                              pol_a);
-                    if (SWIGLU) {
-                        tma_load_2d(b, &tm_w, &full[stage], kx, wrow, pol_w);
-                        tma_load_2d(b + (P_BN / 2) * 128, &tm_w, &full[stage], kx, wrow + UP_OFF,
+                    (void)a2;
+                    tma_load_2d(a1, tm_a, &full[stage], kx, ti.m0, pol_a);
+                    if (SWIGLU) {          // gate rows and up rows in one 3-D copy
+                        tma_load_3d(b, &tm_w, &full[stage], kx, ti.nt * n_per_tile, 2 * ti.g,
                                     pol_w);
                     } else {
                         tma_load_2d(b, &tm_w, &full[stage], kx, wrow, pol_w);
@@ -305,17 +295,20 @@ template <bool SWIGLU>
 moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, int G, int M,
                         int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
                         cudaStream_t stream) {
-    CUtensorMap tm_act, tm_act128, tm_w;
-    if (!encode_bf16_2d(&tm_act, act, K, M, TC_ABOX)) return MOE_ERR_CUDA;
-    if (!encode_bf16_2d(&tm_act128, act, K, M, TC_BM)) return MOE_ERR_CUDA;
-    if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, SWIGLU ? P_BN / 2 : P_BN))
+    CUtensorMap tm_act, tm_act32, tm_act64, tm_act128, tm_act256, tm_w;
+    if (!encode_bf16_2d(&tm_act, act, K, M, 16) || !encode_bf16_2d(&tm_act32, act, K, M, 32) ||
+        !encode_bf16_2d(&tm_act64, act, K, M, 64) || !encode_bf16_2d(&tm_act128, act, K, M, 128) ||
+        !encode_bf16_2d(&tm_act256, act, K, M, 256))
+        return MOE_ERR_CUDA;
+    if (SWIGLU ? !encode_gate_up_3d(&tm_w, w, K, UP_OFF, G, P_BN / 2)
+               : !encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, P_BN))
         return MOE_ERR_CUDA;
     const size_t smem = PCfg::smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
     static int attr_done[64] = {0};
     if (!raise_smem_limit(tc_grouped_gemm_256<SWIGLU>, attr_done)) return MOE_ERR_CUDA;
     launch(tc_grouped_gemm_256<SWIGLU>, sm_count(), P_THREADS, smem, stream, tm_act, tm_act128,
-           tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
+           tm_w, tm_act32, tm_act64, tm_act256, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
 }
 

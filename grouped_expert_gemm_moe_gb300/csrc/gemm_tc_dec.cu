@@ -176,7 +176,6 @@ __global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
             uint64_t *empty = W8 ? q_empty : a_empty;
             uint8_t *ring = W8 ? sQ : sA;
             constexpr int STAGE = W8 ? C::RAW_BYTES : C::A_BYTES;
-            constexpr int ROW = W8 ? TC_BK : TC_BK * 2;     // bytes per weight row in a stage
             int i = 0;
             uint32_t ph = 0, filled = 0, fill_par = 0;
             bool ok = true;
@@ -187,10 +186,9 @@ __global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
                     if (!mbar_wait(&empty[i], ph ^ 1u, dev_error)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[i], STAGE);
                     uint8_t *dst = ring + i * STAGE;
-                    if (SWIGLU) {
-                        tma_load_2d(dst, &tm_w, &full[i], kb * TC_BK, wrow, pol);
-                        tma_load_2d(dst + 64 * ROW, &tm_w, &full[i], kb * TC_BK, wrow + UP_OFF,
-                                    pol);
+                    if (SWIGLU) {      // gate rows and up rows in one 3-D copy
+                        tma_load_3d(dst, &tm_w, &full[i], kb * TC_BK, ti.nt * n_per_tile,
+                                    2 * ti.g, pol);
                     } else {
                         tma_load_2d(dst, &tm_w, &full[i], kb * TC_BK, wrow, pol);
                     }
@@ -356,11 +354,12 @@ static moe_status launch_dec_tn(const void *tok, const void *w, const float *sca
     using C = DecCfg<W8, TN>;
     CUtensorMap tm_tok, tm_w;
     if (!encode_bf16_2d(&tm_tok, tok, K, M, TN)) return MOE_ERR_CUDA;
-    const uint32_t wbox = SWIGLU ? 64 : DEC_BM;
-    if (W8) {
-        if (!encode_u8_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, wbox)) return MOE_ERR_CUDA;
+    if (SWIGLU) {
+        if (!encode_gate_up_3d(&tm_w, w, K, UP_OFF, G, DEC_BM / 2, W8)) return MOE_ERR_CUDA;
+    } else if (W8) {
+        if (!encode_u8_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, DEC_BM)) return MOE_ERR_CUDA;
     } else {
-        if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, wbox)) return MOE_ERR_CUDA;
+        if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, DEC_BM)) return MOE_ERR_CUDA;
     }
     const size_t smem = C::smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;

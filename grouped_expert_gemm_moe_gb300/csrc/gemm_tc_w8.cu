@@ -48,6 +48,8 @@ template <bool SWIGLU>
 __global__ void __launch_bounds__(W8_THREADS, 1)
     tc_grouped_gemm_w8(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_act128,
+                       const __grid_constant__ CUtensorMap tm_act32,
+                       const __grid_constant__ CUtensorMap tm_act64,
                        const __grid_constant__ CUtensorMap tm_q, const float *__restrict__ scales,
                        const int32_t *__restrict__ offsets, int G, int M, int K, int R, int NOUT,
                        int UP_OFF, uint16_t *__restrict__ out, int32_t *dev_error) {
@@ -97,6 +99,8 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_act32);
+        prefetch_tmap(&tm_act64);
         prefetch_tmap(&tm_act128);
         prefetch_tmap(&tm_q);
     }
@@ -122,19 +126,16 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
                 // a tile with more than 64 rows takes one 128-row box; a smaller
                 // one only the 16-row boxes it needs (rows past the group are
                 // loaded but never stored)
-                const bool full_box = ti.nrows > 64;
-                const int nbox = full_box ? TC_BM / TC_ABOX : (ti.nrows + TC_ABOX - 1) / TC_ABOX;
-                const uint32_t bytes = nbox * TC_ABOX * TC_BK * 2;
+                const int abox = ti.nrows <= 16 ? 16 : ti.nrows <= 32 ? 32
+                                                     : ti.nrows <= 64 ? 64 : 128;
+                const CUtensorMap *tm_a = abox == 16 ? &tm_act : abox == 32 ? &tm_act32
+                                        : abox == 64 ? &tm_act64 : &tm_act128;
+                const uint32_t bytes = abox * TC_BK * 2;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&ab_empty[s], ph ^ 1u, dev_error)) { ok = false; break; }
                     mbar_arrive_expect_tx(&a_full[s], bytes);
                     uint8_t *a = sA + s * C::A_BYTES;
-                    if (full_box)
-                        tma_load_2d(a, &tm_act128, &a_full[s], kb * TC_BK, ti.m0, pol);
-                    else
-                        for (int bx = 0; bx < nbox; ++bx)
-                            tma_load_2d(a + bx * TC_ABOX * 128, &tm_act, &a_full[s], kb * TC_BK,
-                                        ti.m0 + bx * TC_ABOX, pol);
+                    tma_load_2d(a, tm_a, &a_full[s], kb * TC_BK, ti.m0, pol);
                     filled |= 1u << s;
                     fill_par = (fill_par & ~(1u << s)) | (ph << s);
                     if (++s == S) { s = 0; ph ^= 1u; }
@@ -158,10 +159,9 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
                     if (!mbar_wait(&q_empty[r], ph ^ 1u, dev_error)) { ok = false; break; }
                     mbar_arrive_expect_tx(&q_full[r], C::RAW_BYTES);
                     uint8_t *q = sQ + r * C::RAW_BYTES;
-                    if (SWIGLU) {
-                        tma_load_2d(q, &tm_q, &q_full[r], kb * TC_BK, wrow, pol);
-                        tma_load_2d(q + (BN / 2) * TC_BK, &tm_q, &q_full[r], kb * TC_BK,
-                                    wrow + UP_OFF, pol);
+                    if (SWIGLU) {      // gate rows and up rows in one 3-D copy
+                        tma_load_3d(q, &tm_q, &q_full[r], kb * TC_BK, ti.nt * n_per_tile,
+                                    2 * ti.g, pol);
                     } else {
                         tma_load_2d(q, &tm_q, &q_full[r], kb * TC_BK, wrow, pol);
                     }
@@ -331,18 +331,20 @@ static moe_status launch_tc_w8(const void *act, const int8_t *q, const float *sc
     if (tile == TILE_DEC16 || tile == TILE_DEC32 || tile == TILE_DEC64)
         return launch_dec<SWIGLU, true>(dec_tn(tile), act, q, scales, offsets, G, M, K, R, NOUT,
                                         UP_OFF, out, dev_error, stream);
-    CUtensorMap tm_act, tm_q;
-    CUtensorMap tm_act128;
-    if (!encode_bf16_2d(&tm_act, act, K, M, TC_ABOX)) return MOE_ERR_CUDA;
-    if (!encode_bf16_2d(&tm_act128, act, K, M, TC_BM)) return MOE_ERR_CUDA;
-    if (!encode_u8_2d(&tm_q, q, K, static_cast<uint64_t>(G) * R, SWIGLU ? W8_BN / 2 : W8_BN))
+    CUtensorMap tm_act, tm_act32, tm_act64, tm_act128, tm_q;
+    if (!encode_bf16_2d(&tm_act, act, K, M, 16) || !encode_bf16_2d(&tm_act32, act, K, M, 32) ||
+        !encode_bf16_2d(&tm_act64, act, K, M, 64) || !encode_bf16_2d(&tm_act128, act, K, M, TC_BM))
+        return MOE_ERR_CUDA;
+    if (SWIGLU ? !encode_gate_up_3d(&tm_q, q, K, UP_OFF, G, W8_BN / 2, true)
+               : !encode_u8_2d(&tm_q, q, K, static_cast<uint64_t>(G) * R, W8_BN))
         return MOE_ERR_CUDA;
     const size_t smem = W8Cfg::smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
     static int attr_done[64] = {0};
     if (!raise_smem_limit(tc_grouped_gemm_w8<SWIGLU>, attr_done)) return MOE_ERR_CUDA;
     launch(tc_grouped_gemm_w8<SWIGLU>, sm_count(), W8_THREADS, smem, stream, 
-        tm_act, tm_act128, tm_q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
+        tm_act, tm_act128, tm_act32, tm_act64, tm_q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out,
+        dev_error);
     return launch_status();
 }
 

@@ -11,7 +11,6 @@ namespace moe {
 constexpr int TC_BM = 128;        // token rows per tile (MMA M)
 constexpr int TC_BK = 64;         // K per stage: one 128-byte swizzle row of bf16
 constexpr int TC_THREADS = 192;   // 6 warps
-constexpr int TC_ABOX = 16;       // rows per activation TMA box
 
 struct TileInfo {
     int g, nt, m0, nrows;
@@ -156,6 +155,26 @@ inline bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, u
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The gate/up weights [G, 2, I, K] bf16 (rows 0..I-1 gate, I..2I-1 up of
+// each group) as a 3-D tensor {K, I, 2G}: one box [2][rows][64] brings the
+// gate rows and the matching up rows of a tile in a single copy, laid out
+// as two 2-D boxes would be (gate rows, then up rows), 128-byte swizzle.
+// int8 = true: the same for int8 weights (64-byte rows, no swizzle).
+inline bool encode_gate_up_3d(CUtensorMap *map, const void *base, uint64_t K, uint64_t I,
+                              uint64_t G, uint32_t rows, bool int8 = false) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const uint64_t esz = int8 ? 1 : 2;
+    const cuuint64_t dims[3] = {K, I, 2 * G};
+    const cuuint64_t strides[2] = {K * esz, I * K * esz};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(TC_BK), rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
