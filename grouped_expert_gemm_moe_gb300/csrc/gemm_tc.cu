@@ -304,23 +304,20 @@ moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, 
                         cudaStream_t stream);
 
 // Tile shape per call, from the mean rows per group (M / G), chosen from
-// GB300 measurements of the OLMoE-shaped layer (bf16 and int8 weights):
-//   <= 8 rows  : 128 x 128 tiles (a decode batch: every weight tile is read
-//                once either way, and this kernel's hand-offs are cheapest);
-//   <= 20 / 48 rows: weight-row tiles (gemm_tc_dec.cu) with token blocks of
-//                32 / 64 rows: the MMA's 128 rows are weight rows, so no
-//                tensor-core time goes to empty token rows (7-8 % faster than
-//                128 x 128 at 16 and 32 rows per group);
-//   <= 64 rows : 128 x 128 tiles (twice the tiles of 128 x 256, which evens
-//                out the last wave when the groups are small);
-//   <= 512 rows: 128 x 256 tiles;
-//   more       : 256-row token blocks x 256 weight rows (gemm_tc256.cu), which
-//                need a third fewer operand bytes per FLOP and win once most
-//                groups fill several blocks (0.73 of bf16 peak at 1024 rows
-//                per group against 0.65 for 128 x 256).
+// GB300 measurements of the OLMoE- and DeepSeek-shaped layers:
+//   <= 64 rows : 128 x 128 tiles.  (The weight-row tiles of gemm_tc_dec.cu,
+//                which spend no MMA rows on empty token rows, measured equal
+//                or slower for bf16 once every stage took one copy per
+//                operand; int8 weights keep them for 8-48 rows, see
+//                pick_tile_w8.)
+//   more       : 128 x 256 tiles (0.75 of bf16 peak at 1024 rows per group).
+//                The 256-row token blocks of gemm_tc256.cu (a third fewer
+//                operand bytes per FLOP) measured 5-16 % slower at 32-1024
+//                rows per group once both kernels took one copy per operand
+//                per stage, so the choice never falls on them.
 // MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill in the environment
 // overrides the choice.
-int pick_tile(int M, int G) {
+static int forced_tile() {
     static const int forced = [] {
         const char *v = getenv("MOE_GEMM_TILE");
         if (!v) return -1;
@@ -332,14 +329,24 @@ int pick_tile(int M, int G) {
         if (!strcmp(v, "prefill")) return static_cast<int>(TILE_PREFILL);
         return -1;
     }();
-    if (forced >= 0) return forced;
+    return forced;
+}
+
+int pick_tile(int M, int G) {
+    if (forced_tile() >= 0) return forced_tile();
+    const int64_t m = M, g = G;
+    return m <= 64 * g ? TILE_128 : TILE_256;
+}
+
+// int8 weights: the weight-row tiles for 8-48 rows per group (the 128-token
+// int8 kernel widens 256 weight rows per k-step for a handful of tokens).
+int pick_tile_w8(int M, int G) {
+    if (forced_tile() >= 0) return forced_tile();
     const int64_t m = M, g = G;
     if (m <= 8 * g) return TILE_128;
     if (m <= 20 * g) return TILE_DEC32;
     if (m <= 48 * g) return TILE_DEC64;
-    if (m <= 64 * g) return TILE_128;
-    if (m <= 512 * g) return TILE_256;
-    return TILE_PREFILL;
+    return TILE_256;
 }
 }  // namespace moe
 

@@ -38,18 +38,22 @@ namespace moe {
 
 constexpr int DEC_BM = 128;          // weight rows per tile (MMA M)
 
-template <bool W8, int TN>
+// KP: 64-element k-blocks per stage (2 for bf16 weights when K % 128 == 0:
+// one copy per operand then moves twice the bytes; the ring's pace is set
+// by copies and hand-offs per stage more than by bytes).
+template <bool W8, int TN, int KP = 1>
 struct DecCfg {
-    static constexpr int A_BYTES = DEC_BM * TC_BK * 2;          // bf16 weight tile
-    static constexpr int B_BYTES = TN * TC_BK * 2;              // token tile
+    static_assert(KP == 1 || (KP == 2 && !W8), "int8 stages hold one k-block");
+    static constexpr int A_BYTES = DEC_BM * TC_BK * 2 * KP;     // bf16 weight tile
+    static constexpr int B_BYTES = TN * TC_BK * 2 * KP;         // token tile
     static constexpr int RAW_BYTES = DEC_BM * TC_BK;            // int8 weight tile
     // Rings (sized to fit 227 KB of shared memory with G = 1024 groups):
     // token tiles TOK_STAGES deep, weight tiles STAGES deep, raw int8 tiles
     // RAW_STAGES deep.  The token ring is separate and deep because token
     // tiles come from L2 for every k-step: a short shared ring would put
     // that L2 round trip into every k-step's hand-off.
-    static constexpr int TOK_STAGES = TN <= 32 ? 16 : 8;
-    static constexpr int STAGES = W8 ? 4 : (TN <= 16 ? 10 : 8);
+    static constexpr int TOK_STAGES = KP == 2 ? (TN <= 32 ? 8 : 4) : (TN <= 32 ? 16 : 8);
+    static constexpr int STAGES = W8 ? 4 : KP == 2 ? (TN <= 16 ? 5 : 4) : (TN <= 16 ? 10 : 8);
     static constexpr int RAW_STAGES = W8 ? (TN <= 16 ? 12 : TN <= 32 ? 10 : 8) : 0;
     static constexpr int XBUF_BYTES = 64 * TN * 4;              // up values, fp32
     static constexpr uint32_t TMEM_COLS = 2 * TN < 32 ? 32 : 2 * TN;
@@ -69,13 +73,13 @@ struct DecCfg {
 // SWIGLU: out = h [M, NOUT=I], weights [G*2I, K=H] (up rows at +UP_OFF = I).
 // PLAIN : out = y [M, NOUT=H], weights [G*H,  K=I].
 // R = weight rows per group.  scales: int8 only, [G*R] fp32.
-template <bool SWIGLU, bool W8, int TN>
-__global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
+template <bool SWIGLU, bool W8, int TN, int KP>
+__global__ void __launch_bounds__(DecCfg<W8, TN, KP>::THREADS, 1)
     tc_grouped_gemm_dec(const __grid_constant__ CUtensorMap tm_tok,
                         const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ scales,
                         const int32_t *__restrict__ offsets, int G, int M, int K, int R,
                         int NOUT, int UP_OFF, uint16_t *__restrict__ out, int32_t *dev_error) {
-    using C = DecCfg<W8, TN>;
+    using C = DecCfg<W8, TN, KP>;
     constexpr int S = C::STAGES;
     constexpr int TS = C::TOK_STAGES;
     constexpr int RS = C::RAW_STAGES > 0 ? C::RAW_STAGES : 1;
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = lane_id();
     const int n_per_tile = SWIGLU ? DEC_BM / 2 : DEC_BM;
     const int n_tiles = (NOUT + n_per_tile - 1) / n_per_tile;
-    const int KB = (K + TC_BK - 1) / TC_BK;
+    const int KB = (K + TC_BK * KP - 1) / (TC_BK * KP);     // stages per tile
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < TS; ++i) {
@@ -156,7 +160,12 @@ __global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&b_empty[i], ph ^ 1u, dev_error)) { ok = false; break; }
                     mbar_arrive_expect_tx(&b_full[i], C::B_BYTES);
-                    tma_load_2d(sB + i * C::B_BYTES, &tm_tok, &b_full[i], kb * TC_BK, ti.m0, pol);
+                    if (KP == 2)
+                        tma_load_3d(sB + i * C::B_BYTES, &tm_tok, &b_full[i], 0, ti.m0, 2 * kb,
+                                    pol);
+                    else
+                        tma_load_2d(sB + i * C::B_BYTES, &tm_tok, &b_full[i], kb * TC_BK, ti.m0,
+                                    pol);
                     filled |= 1u << i;
                     fill_par = (fill_par & ~(1u << i)) | (ph << i);
                     if (++i == TS) { i = 0; ph ^= 1u; }
@@ -186,7 +195,13 @@ __global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
                     if (!mbar_wait(&empty[i], ph ^ 1u, dev_error)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[i], STAGE);
                     uint8_t *dst = ring + i * STAGE;
-                    if (SWIGLU) {      // gate rows and up rows in one 3-D copy
+                    if (KP == 2) {     // two k-blocks (and gate + up rows) in one copy
+                        if (SWIGLU)
+                            tma_load_4d(dst, &tm_w, &full[i], 0, ti.nt * n_per_tile, 2 * ti.g,
+                                        2 * kb, pol);
+                        else
+                            tma_load_3d(dst, &tm_w, &full[i], 0, wrow, 2 * kb, pol);
+                    } else if (SWIGLU) {   // gate rows and up rows in one 3-D copy
                         tma_load_3d(dst, &tm_w, &full[i], kb * TC_BK, ti.nt * n_per_tile,
                                     2 * ti.g, pol);
                     } else {
@@ -244,10 +259,13 @@ __global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
                     const uint32_t a_addr = smem_u32(sA + s * C::A_BYTES);
                     const uint32_t b_addr = smem_u32(sB + tb * C::B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < TC_BK / 16; ++kk)
-                        tc_mma_bf16(d_tmem, sw128_kmajor_desc(a_addr + kk * 32),
-                                    sw128_kmajor_desc(b_addr + kk * 32), idesc,
-                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                    for (int kq = 0; kq < KP; ++kq)
+#pragma unroll
+                        for (int kk = 0; kk < TC_BK / 16; ++kk)
+                            tc_mma_bf16(d_tmem,
+                                        sw128_kmajor_desc(a_addr + kq * DEC_BM * 128 + kk * 32),
+                                        sw128_kmajor_desc(b_addr + kq * TN * 128 + kk * 32), idesc,
+                                        (kb > 0 || kq > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&a_empty[s]);
                     tc_commit(&b_empty[tb]);
                     if (++s == S) { s = 0; ph ^= 1u; }
@@ -346,28 +364,50 @@ __global__ void __launch_bounds__(DecCfg<W8, TN>::THREADS, 1)
 
 // ------------------------------------------------------------------ host
 
-template <bool SWIGLU, bool W8, int TN>
+template <bool SWIGLU, bool W8, int TN, int KP>
 static moe_status launch_dec_tn(const void *tok, const void *w, const float *scales,
                                 const int32_t *offsets, int G, int M, int K, int R, int NOUT,
                                 int UP_OFF, uint16_t *out, int32_t *dev_error,
                                 cudaStream_t stream) {
-    using C = DecCfg<W8, TN>;
+    using C = DecCfg<W8, TN, KP>;
     CUtensorMap tm_tok, tm_w;
-    if (!encode_bf16_2d(&tm_tok, tok, K, M, TN)) return MOE_ERR_CUDA;
-    if (SWIGLU) {
-        if (!encode_gate_up_3d(&tm_w, w, K, UP_OFF, G, DEC_BM / 2, W8)) return MOE_ERR_CUDA;
-    } else if (W8) {
-        if (!encode_u8_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, DEC_BM)) return MOE_ERR_CUDA;
+    if (KP == 2) {
+        if (!encode_kpair(&tm_tok, tok, K, M, TN)) return MOE_ERR_CUDA;
+        if (SWIGLU ? !encode_gate_up_kpair(&tm_w, w, K, UP_OFF, G, DEC_BM / 2)
+                   : !encode_kpair(&tm_w, w, K, static_cast<uint64_t>(G) * R, DEC_BM))
+            return MOE_ERR_CUDA;
     } else {
-        if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, DEC_BM)) return MOE_ERR_CUDA;
+        if (!encode_bf16_2d(&tm_tok, tok, K, M, TN)) return MOE_ERR_CUDA;
+        if (SWIGLU) {
+            if (!encode_gate_up_3d(&tm_w, w, K, UP_OFF, G, DEC_BM / 2, W8)) return MOE_ERR_CUDA;
+        } else if (W8) {
+            if (!encode_u8_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, DEC_BM))
+                return MOE_ERR_CUDA;
+        } else {
+            if (!encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, DEC_BM))
+                return MOE_ERR_CUDA;
+        }
     }
     const size_t smem = C::smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
     static int attr_done[64] = {0};
-    if (!raise_smem_limit(tc_grouped_gemm_dec<SWIGLU, W8, TN>, attr_done)) return MOE_ERR_CUDA;
-    launch(tc_grouped_gemm_dec<SWIGLU, W8, TN>, sm_count(), C::THREADS, smem, stream, tm_tok,
+    if (!raise_smem_limit(tc_grouped_gemm_dec<SWIGLU, W8, TN, KP>, attr_done))
+        return MOE_ERR_CUDA;
+    launch(tc_grouped_gemm_dec<SWIGLU, W8, TN, KP>, sm_count(), C::THREADS, smem, stream, tm_tok,
            tm_w, scales, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
     return launch_status();
+}
+
+template <bool SWIGLU, bool W8, int TN>
+static moe_status launch_dec_kp(const void *tok, const void *w, const float *scales,
+                                const int32_t *offsets, int G, int M, int K, int R, int NOUT,
+                                int UP_OFF, uint16_t *out, int32_t *dev_error,
+                                cudaStream_t stream) {
+    if (!W8 && K % 128 == 0)
+        return launch_dec_tn<SWIGLU, W8, TN, W8 ? 1 : 2>(tok, w, scales, offsets, G, M, K, R,
+                                                          NOUT, UP_OFF, out, dev_error, stream);
+    return launch_dec_tn<SWIGLU, W8, TN, 1>(tok, w, scales, offsets, G, M, K, R, NOUT, UP_OFF,
+                                            out, dev_error, stream);
 }
 
 // Token-block height TN for the decode kernel (16, 32 or 64).
@@ -377,13 +417,13 @@ moe_status launch_dec(int tn, const void *tok, const void *w, const float *scale
                       uint16_t *out, int32_t *dev_error, cudaStream_t stream) {
     switch (tn) {
         case 16:
-            return launch_dec_tn<SWIGLU, W8, 16>(tok, w, scales, offsets, G, M, K, R, NOUT, UP_OFF,
+            return launch_dec_kp<SWIGLU, W8, 16>(tok, w, scales, offsets, G, M, K, R, NOUT, UP_OFF,
                                                  out, dev_error, stream);
         case 32:
-            return launch_dec_tn<SWIGLU, W8, 32>(tok, w, scales, offsets, G, M, K, R, NOUT, UP_OFF,
+            return launch_dec_kp<SWIGLU, W8, 32>(tok, w, scales, offsets, G, M, K, R, NOUT, UP_OFF,
                                                  out, dev_error, stream);
         default:
-            return launch_dec_tn<SWIGLU, W8, 64>(tok, w, scales, offsets, G, M, K, R, NOUT, UP_OFF,
+            return launch_dec_kp<SWIGLU, W8, 64>(tok, w, scales, offsets, G, M, K, R, NOUT, UP_OFF,
                                                  out, dev_error, stream);
     }
 }

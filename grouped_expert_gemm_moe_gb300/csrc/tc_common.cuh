@@ -178,6 +178,37 @@ inline bool encode_gate_up_3d(CUtensorMap *map, const void *base, uint64_t K, ui
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Two 64-element k-blocks per copy.  A bf16 matrix [rows, K] (K a multiple
+// of 128) viewed as {64, rows, K/64}: the box {64, box_rows, 2} lands in
+// shared memory as two 128-byte-swizzled [box_rows][64] tiles, k-block by
+// k-block.  With gate_up: the [G, 2, I, K] gate/up weights viewed as {64, I,
+// 2G, K/64}, box {64, box_rows, 2, 2}: per k-block the gate rows then the up
+// rows.  (K % 128 != 0 would make the last k-block wrap into the next row.)
+inline bool encode_kpair(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows,
+                         uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc || K % 128 != 0) return false;
+    const cuuint64_t dims[3] = {64, rows, K / 64};
+    const cuuint64_t strides[2] = {K * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+inline bool encode_gate_up_kpair(CUtensorMap *map, const void *base, uint64_t K, uint64_t I,
+                                 uint64_t G, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc || K % 128 != 0) return false;
+    const cuuint64_t dims[4] = {64, I, 2 * G, K / 64};
+    const cuuint64_t strides[3] = {K * 2, I * K * 2, 128};
+    const cuuint32_t box[4] = {64, box_rows, 2, 2};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D uint8 tensor [outer, inner] row-major, box [box_outer, 64 bytes], no swizzle.
 inline bool encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
                          uint32_t box_outer) {
@@ -210,6 +241,7 @@ inline bool raise_smem_limit(Kernel kernel, int *done_per_device) {
 // Tile shapes of the grouped GEMMs (gemm_tc.cu picks one per call).
 enum { TILE_DEC16 = 0, TILE_DEC32, TILE_DEC64, TILE_128, TILE_256, TILE_PREFILL };
 int pick_tile(int M, int G);
+int pick_tile_w8(int M, int G);
 inline int dec_tn(int tile) { return tile == TILE_DEC16 ? 16 : tile == TILE_DEC32 ? 32 : 64; }
 
 // Weight-row tiles for decode-sized groups (gemm_tc_dec.cu); scales: int8 only.
