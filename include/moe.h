@@ -318,6 +318,38 @@ moe_status moe_combine_capped(const uint16_t *y_perm, const int32_t *row_of_slot
                               int32_t *dev_error, cudaStream_t stream);
 
 /*
+ * moe_decode_workspace_size -- bytes of device workspace moe_decode_layer
+ * needs: a grid-barrier word plus the hidden rows h [M,I] and the expert
+ * outputs y [M,H] (bf16), M = T*k + S*T.  0 for invalid sizes.
+ */
+size_t moe_decode_workspace_size(int T, int E, int S, int k, int H, int I);
+
+/*
+ * moe_decode_layer -- a whole decode-sized MoE layer in one cooperative
+ * launch: moe_route, the stable sort of the T*k slots by expert, the grouped
+ * GEMV gate/up + SwiGLU, the grouped GEMV down and moe_combine, with grid
+ * barriers between the phases.  The pages' kernels trail most at one token
+ * ("dispatch", Phase 6 pull request, Summary), where a layer is several
+ * short launches around one weight stream; here it is one.
+ * The result is the same bytes as moe_route -> moe_permute ->
+ * moe_grouped_gemv -> moe_combine on the same inputs.
+ * logits: [T,E] fp32; x: [T,H] bf16 (read by token, no gathered copy);
+ * w_gu: [E+S,2I,H]; w_down: [E+S,H,I] bf16; residual: [T,H] bf16 or NULL;
+ * out: [T,H] bf16 (may alias residual); topk_ids: [T,k] int32 and
+ * topk_w: [T,k] fp32 are written (NULL to skip).  workspace: at least
+ * moe_decode_workspace_size bytes, 16-byte aligned, owned by the caller and
+ * not shared with work in flight on another stream.
+ * Limits (else MOE_ERR_UNSUPPORTED): T <= 8, T*k <= 64, S*T <= 64, S <= 32,
+ * E <= 256; H and I multiples of 8.  The grid barriers wait at most 1 s:
+ * on running out a CTA records MOE_ERR_TIMEOUT in dev_error and returns.
+ */
+moe_status moe_decode_layer(const float *logits, const uint16_t *x, int T, int E, int S, int k,
+                            int renormalize, int H, int I, const uint16_t *w_gu,
+                            const uint16_t *w_down, const uint16_t *residual, uint16_t *out,
+                            int32_t *topk_ids, float *topk_w, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_error, cudaStream_t stream);
+
+/*
  * moe_quantize_w8 -- offline, host-side int8 quantisation of expert
  * weights ("dispatch" README, phase 5a: self-computed per-channel scales).
  * w_host: [rows, K] bf16 bits in host memory; q_host: [rows, K] int8 and
