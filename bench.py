@@ -346,11 +346,14 @@ def kernel_roofline(shape, T, n_groups, gate_up_ms, peaks, kind, workload):
             "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
 
 
-def measure_T(layer, shape, T, x, logits, K, W, flush, peaks, workload):
+def measure_T(layer, shape, T, x, logits, K, W, flush, peaks, workload, ffn="auto"):
     """Layer time from K steps of the whole forward pass captured in one
     CUDA graph; the gate/up kernel's time from K further steps recorded as
-    three graphs with events around the gate/up launch."""
-    kind = layer.choose_path(T, x.dtype)
+    three graphs with events around the gate/up launch.  ffn: "auto" (the
+    layer's own choice) or a forced "decode", "gemv" or "gemm"."""
+    kind = layer.choose_path(T, x.dtype) if ffn == "auto" else ffn
+    if kind == "decode" and not layer.decode_layer_ok(T, x.dtype):
+        raise SystemExit(f"--ffn decode: T={T} is outside the fused decode layer's limits")
     cap = layer.capture(x, logits, ffn=kind)
     step = time_graph(cap, K, W, flush)
     ms = statistics.fmean(step)
@@ -387,7 +390,7 @@ def decode_kernel_roofline(shape, T, n_groups, step_ms, peaks, workload):
             "peak_source": f"{peaks['source']} (STREAM copy, burst)"}
 
 
-def e2e_measure(layer, shape, T, inp, K, W, flush):
+def e2e_measure(layer, shape, T, inp, K, W, flush, ffn="auto"):
     """End to end through the public API: pinned host x and logits copied in,
     the captured forward pass, the output copied back, every step."""
     import torch
@@ -399,7 +402,7 @@ def e2e_measure(layer, shape, T, inp, K, W, flush):
     l_dev = torch.empty_like(inp.logits, device=dev)
     x_dev.copy_(x_host)
     l_dev.copy_(l_host)
-    cap = layer.capture(x_dev, l_dev)
+    cap = layer.capture(x_dev, l_dev, ffn=ffn)
 
     def step():
         x_dev.copy_(x_host, non_blocking=True)
@@ -598,7 +601,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     # correctness first: one pass, checked against the oracle before timing
-    out0 = layer.forward(inp.x, inp.logits).clone()
+    out0 = layer.forward(inp.x, inp.logits, ffn=args.ffn).clone()
     layer.check()
     base = None
     if rank == 0 and world == 1:
@@ -615,7 +618,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_wall0 = time.time()
     m = measure_T(layer, shape, T, inp.x, inp.logits, args.steps, args.warmup, flush, peaks,
-                  args.workload)
+                  args.workload, args.ffn)
     torch.cuda.synchronize()
     barrier(world)
     t_wall1 = time.time()
@@ -641,7 +644,8 @@ def run_ours(args):
     if world == 1 and not args.no_rows:
         rows = other_rows(dev, args.steps, args.warmup, flush, peaks)
 
-    e2e_ms, h2d, d2h, out_e2e = e2e_measure(layer, shape, T, inp, args.steps, args.warmup, flush)
+    e2e_ms, h2d, d2h, out_e2e = e2e_measure(layer, shape, T, inp, args.steps, args.warmup, flush,
+                                            m["kind"])
     layer.check()
     e2e_sec = reduce_max(e2e_ms * args.steps / 1e3, world, dev)
     if not torch.equal(out_e2e.to(dev), out0):
@@ -742,6 +746,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ffn", choices=("auto", "decode", "gemv", "gemm"), default="auto",
+                    help="FFN path of the workload's layer: the layer's own choice, or "
+                         "forced (to time or profile one path)")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the int8 and 16-layer stack measurements of other_rows")
     args = ap.parse_args(argv)
