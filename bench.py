@@ -553,36 +553,47 @@ def run_oracle_tokens(inp, host, tokens, wbits, nthreads=0):
                             nthreads=nthreads)
 
 
-def cpu_baseline(inp, gpu_out, max_tokens=64):
-    """The oracle, as it stands, on the host cores over (up to) the first
-    max_tokens tokens of the batch; also the parity gate of the bench: a
-    GPU result that disagrees with it is not timed."""
+def cpu_baseline(inp, gpu_out, min_seconds=10.0, min_seconds_1_thread=2.0):
+    """The oracle, as it stands, on the host cores: route + permute + layer
+    of every token of the batch, repeated until at least min_seconds of
+    work have run; also the parity gate of the bench: a GPU result that
+    disagrees with it (on any token) is not timed."""
     import numpy as np
 
     import oracle
     from grouped_expert_gemm_moe_gb300 import workloads as W
     T = inp.T
-    tokens = np.arange(min(T, max_tokens))
+    tokens = np.arange(T)
     host = oracle_sample(inp, tokens)
     wbits = (W.bf16_bits(inp.w_gu), W.bf16_bits(inp.w_down))
     t0 = time.perf_counter()
     y = run_oracle_tokens(inp, host, tokens, wbits)
     sec = time.perf_counter() - t0
+    reps = 1
+    while sec < min_seconds:
+        t0 = time.perf_counter()
+        run_oracle_tokens(inp, host, tokens, wbits)
+        sec += time.perf_counter() - t0
+        reps += 1
     got = gpu_out.float().cpu().numpy().astype(np.float64)[tokens]
     rel = float(np.linalg.norm(got - y) / np.linalg.norm(y))
     mx = float(np.abs(got - y).max() / np.abs(y).max())
     cores = min(len(tokens), oracle.num_threads())
-    # the same oracle on one thread, for scale (a smaller sample)
+    # the same oracle on one thread, for scale (a few tokens, repeated)
     t1 = tokens[:min(len(tokens), 4)]
     h1 = oracle_sample(inp, t1)
-    t0 = time.perf_counter()
-    run_oracle_tokens(inp, h1, t1, wbits, nthreads=1)
-    sec1 = time.perf_counter() - t0
-    return dict(value=round(len(tokens) / sec, 3), unit=UNIT, cores=cores, kind="oracle",
-                sample=f"route+permute+layer of tokens 0..{len(tokens) - 1} of the timed batch "
-                       f"({len(tokens)} tokens, {sec:.2f} s)",
-                value_1_thread=round(len(t1) / sec1, 3),
-                sample_1_thread=f"tokens 0..{len(t1) - 1} on one thread ({sec1:.2f} s)",
+    sec1, reps1 = 0.0, 0
+    while sec1 < min_seconds_1_thread:
+        t0 = time.perf_counter()
+        run_oracle_tokens(inp, h1, t1, wbits, nthreads=1)
+        sec1 += time.perf_counter() - t0
+        reps1 += 1
+    return dict(value=round(reps * len(tokens) / sec, 3), unit=UNIT, cores=cores, kind="oracle",
+                sample=f"route+permute+layer of all {len(tokens)} tokens of the timed batch, "
+                       f"{reps} times ({sec:.1f} s)",
+                value_1_thread=round(reps1 * len(t1) / sec1, 3),
+                sample_1_thread=f"tokens 0..{len(t1) - 1} on one thread, {reps1} times "
+                                f"({sec1:.1f} s)",
                 parity={"rel_frobenius": rel, "max_rel": mx, "ok": rel <= 5e-3 and mx <= 2e-2})
 
 
