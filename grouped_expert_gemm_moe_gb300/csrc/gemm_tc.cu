@@ -315,7 +315,7 @@ moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, 
 //                operand bytes per FLOP) measured 5-16 % slower at 32-1024
 //                rows per group once both kernels took one copy per operand
 //                per stage, so the choice never falls on them.
-// MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill in the environment
+// MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill|pair in the environment
 // overrides the choice.
 static int forced_tile() {
     static const int forced = [] {
@@ -327,6 +327,7 @@ static int forced_tile() {
         if (!strcmp(v, "128")) return static_cast<int>(TILE_128);
         if (!strcmp(v, "256")) return static_cast<int>(TILE_256);
         if (!strcmp(v, "prefill")) return static_cast<int>(TILE_PREFILL);
+        if (!strcmp(v, "pair")) return static_cast<int>(TILE_PAIR);
         return -1;
     }();
     return forced;
@@ -366,6 +367,9 @@ static moe_status launch_tc_bn(const void *act, const void *w, const int32_t *of
                                           dev_error, stream);
         case TILE_256:
             return launch_tc<SWIGLU, 256>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
+                                          dev_error, stream);
+        case TILE_PAIR:
+            return launch_tc_pair<SWIGLU>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
                                           dev_error, stream);
         default:
             return launch_tc256<SWIGLU>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,

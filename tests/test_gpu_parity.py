@@ -340,11 +340,12 @@ def test_fused_route_permute_limits_and_nan(B, L):
                             torch.empty((1200, 256), dtype=torch.bfloat16, device=DEV))
 
 
-@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "128", "256", "prefill"])
+@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "128", "256", "prefill", "pair"])
 def test_gemm_tile_shapes_agree(B, L, tile):
     """Every tile shape of the tcgen05 GEMM (weight-row tiles with 16/32/64-
-    token blocks, 128 x 128, 128 x 256, 256-row prefill blocks; normally
-    chosen per call from the rows per group) gives results within tolerance
+    token blocks, 128 x 128, 128 x 256, 256-row prefill blocks, 256 x 256
+    tiles on CTA pairs; normally chosen per call from the rows per group)
+    gives results within tolerance
     of the oracle on a DeepSeek-shaped batch (zipf routing: group sizes from
     a few rows to the 512-row shared experts)."""
     import subprocess, sys, os
