@@ -126,6 +126,35 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// The same for a 3-D box (x = k, y = row, z = plane).
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int x, int y, int z,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster),
+        "l"(policy)
+        : "memory");
+}
+
+// Rows of a pair tile in CTA r: a tile of more than 128 rows is an M = 256
+// MMA with 128 rows per CTA; a group's last m-block of at most 128 rows is
+// an M = 128 MMA with 64 rows per CTA (half the tensor work).
+struct PairRows {
+    bool half;
+    int r0, r1;       // rows in CTA 0 / CTA 1
+    int per_cta;      // 128 or 64
+};
+__device__ __forceinline__ PairRows pair_rows(int nrows) {
+    PairRows p;
+    p.half = nrows <= 128;
+    p.per_cta = p.half ? 64 : 128;
+    p.r0 = min(nrows, p.per_cta);
+    p.r1 = nrows - p.r0;
+    return p;
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot) {   // one warp in each CTA
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(slot)),
@@ -254,20 +283,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             for (int t = t_first; t < total && ok; t += t_step) {
                 const TileInfo ti = decode_tile(t, s_tile, s_off, G, PAIR_BM);
-                const int rows0 = min(ti.nrows, 128);
-                const int rows1 = ti.nrows - rows0;
-                const int my_rows = leader ? rows0 : rows1;
+                const PairRows pr = pair_rows(ti.nrows);
+                const int my_rows = leader ? pr.r0 : pr.r1;
                 const int abox = abox_rows(my_rows);
                 const CUtensorMap *tm_a = abox == 16 ? &tm_act16 : abox == 32 ? &tm_act32
                                         : abox == 64 ? &tm_act64 : &tm_act128;
                 const uint32_t bytes = static_cast<uint32_t>(
-                    (abox_rows(rows0) + abox_rows(rows1)) * TC_BK * 2 + 2 * PAIR_B_BYTES);
-                // this CTA's weight rows: gate (CTA 0) or up (CTA 1) rows of the
-                // tile in SwiGLU mode, else rows 128r.. of the tile
-                const int wrow = SWIGLU ? ti.g * R + static_cast<int>(rank) * UP_OFF +
-                                              ti.nt * n_per_tile
+                    (abox_rows(pr.r0) + abox_rows(pr.r1)) * TC_BK * 2 + 2 * PAIR_B_BYTES);
+                // this CTA's weight rows: in SwiGLU mode the gate rows of
+                // features f0 + 64r .. +63 and the matching up rows (one 3-D
+                // box), else rows 128r .. 128r+127 of the tile
+                const int wrow = SWIGLU ? ti.nt * n_per_tile + static_cast<int>(rank) * 64
                                         : ti.g * R + ti.nt * n_per_tile + static_cast<int>(rank) * 128;
-                const int arow = ti.m0 + static_cast<int>(rank) * 128;
+                const int arow = ti.m0 + static_cast<int>(rank) * pr.per_cta;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, dev_error)) {
                         ok = false;
@@ -282,7 +310,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int kx = kb * TC_BK;
                     if (abox > 0)
                         tma_load_2d_pair(sA + stage * PAIR_A_BYTES, tm_a, bar0, kx, arow, pol_a);
-                    tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tm_w, bar0, kx, wrow, pol_w);
+                    if (SWIGLU)
+                        tma_load_3d_pair(sB + stage * PAIR_B_BYTES, &tm_w, bar0, kx, wrow,
+                                         2 * ti.g, pol_w);
+                    else
+                        tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tm_w, bar0, kx, wrow, pol_w);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -297,13 +329,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (CTA 0 only)
         if (leader && lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(PAIR_BM, PAIR_BN);
+            constexpr uint32_t idesc_full = idesc_bf16_f32(PAIR_BM, PAIR_BN);
+            constexpr uint32_t idesc_half = idesc_bf16_f32(PAIR_BM / 2, PAIR_BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int t = t_first; t < total && ok; t += t_step) {
+                const uint32_t idesc =
+                    decode_tile(t, s_tile, s_off, G, PAIR_BM).nrows <= 128 ? idesc_half : idesc_full;
                 if (!mbar_wait_cluster(&acce[acc], acc_phase ^ 1u, dev_error)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
@@ -348,22 +383,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const TileInfo ti = decode_tile(t, s_tile, s_off, G, PAIR_BM);
             if (!mbar_wait(&accf[acc], acc_phase, dev_error)) break;
             tc_fence_after();
-            const int my_rows = leader ? min(ti.nrows, 128) : ti.nrows - min(ti.nrows, 128);
-            const bool valid = row_in_tile < my_rows;
+            // Accumulator layout (per CTA, TMEM columns from tbase):
+            //   M = 256 tile: lane i = row i, columns 0..255 = the tile's 256
+            //     weight rows (SwiGLU: gate f0..63, up f0..63, gate f64..127,
+            //     up f64..127);
+            //   M = 128 tile: lane i < 64 = row i, columns 0..127 = weight rows
+            //     0..127; lane 64 + i = row i, columns 0..127 = weight rows
+            //     128..255.
+            const PairRows pr = pair_rows(ti.nrows);
+            const int my_rows = leader ? pr.r0 : pr.r1;
+            const int row = pr.half ? (row_in_tile & 63) : row_in_tile;
+            const int wpart = pr.half ? (row_in_tile >> 6) : 0;   // which half of the weight rows
+            const bool valid = row < my_rows;
             uint16_t *orow =
-                out + static_cast<int64_t>(ti.m0 + static_cast<int>(rank) * 128 + row_in_tile) *
+                out + static_cast<int64_t>(ti.m0 + static_cast<int>(rank) * pr.per_cta + row) *
                           NOUT;
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * PAIR_BN;
             const int n0 = ti.nt * n_per_tile;
             if (SWIGLU) {
+                // features fb .. fb + nf - 1 of this thread; gate of feature
+                // fb + c at column gc(c), up at gc(c) + 64
+                const int fb = wpart * 64;
+                const int nf = pr.half ? 64 : 128;
 #pragma unroll 1
-                for (int c = 0; c < PAIR_BN / 2; c += 16) {
+                for (int c = 0; c < nf; c += 16) {
+                    const int gcol = c < 64 ? c : c + 64;
                     uint32_t g[16], u[16];
-                    tmem_ld16(tbase + c, g);
-                    tmem_ld16(tbase + PAIR_BN / 2 + c, u);
+                    tmem_ld16(tbase + gcol, g);
+                    tmem_ld16(tbase + gcol + 64, u);
                     tmem_ld_wait();
-                    if (valid && n0 + c < NOUT) {
+                    const int f = n0 + fb + c;
+                    if (valid && f < NOUT) {
                         uint32_t p[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
@@ -373,26 +424,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                              __uint_as_float(u[2 * i + 1]);
                             p[i] = pack_bf16x2(h0, h1);
                         }
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c);
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + f);
                         dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                        if (n0 + c + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                        if (f + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
                     }
                 }
             } else {
+                const int cb = wpart * 128;
+                const int nc = pr.half ? 128 : PAIR_BN;
 #pragma unroll 1
-                for (int c = 0; c < PAIR_BN; c += 16) {
+                for (int c = 0; c < nc; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tbase + c, v);
                     tmem_ld_wait();
-                    if (valid && n0 + c < NOUT) {
+                    const int o = n0 + cb + c;
+                    if (valid && o < NOUT) {
                         uint32_t p[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             p[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
                                                __uint_as_float(v[2 * i + 1]));
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + n0 + c);
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + o);
                         dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                        if (n0 + c + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                        if (o + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
                     }
                 }
             }
@@ -429,7 +483,8 @@ moe_status launch_tc_pair(const void *act, const void *w, const int32_t *offsets
     CUtensorMap tm_act16, tm_act32, tm_act64, tm_act128, tm_w;
     if (!encode_bf16_2d(&tm_act16, act, K, M, 16) || !encode_bf16_2d(&tm_act32, act, K, M, 32) ||
         !encode_bf16_2d(&tm_act64, act, K, M, 64) || !encode_bf16_2d(&tm_act128, act, K, M, 128) ||
-        !encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, 128))
+        !(SWIGLU ? encode_gate_up_3d(&tm_w, w, K, UP_OFF, G, 64)
+                 : encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, 128)))
         return MOE_ERR_CUDA;
     const size_t smem = pair_smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;

@@ -340,8 +340,10 @@ def test_fused_route_permute_limits_and_nan(B, L):
                             torch.empty((1200, 256), dtype=torch.bfloat16, device=DEV))
 
 
-@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "128", "256", "prefill", "pair"])
-def test_gemm_tile_shapes_agree(B, L, tile):
+@pytest.mark.parametrize("tile,case", [(t, ("deepseek", 512, "zipf")) for t in
+                                       ("dec16", "dec32", "dec64", "128", "256", "prefill", "pair")]
+                         + [("pair", ("olmoe", 2048, "uniform")), ("pair", ("olmoe", 700, "zipf"))])
+def test_gemm_tile_shapes_agree(B, L, tile, case):
     """Every tile shape of the tcgen05 GEMM (weight-row tiles with 16/32/64-
     token blocks, 128 x 128, 128 x 256, 256-row prefill blocks, 256 x 256
     tiles on CTA pairs; normally chosen per call from the rows per group)
@@ -356,15 +358,15 @@ def test_gemm_tile_shapes_agree(B, L, tile):
         "from grouped_expert_gemm_moe_gb300.layer import MoELayer\n"
         "sys.path.insert(0, %r)\n"
         "from gpu_helpers import host_inputs, oracle_out, sample_tokens, assert_close, to_np\n"
-        "inp = W.make_layer(W.DEEPSEEK, 512, 'zipf', seed=0, device='cuda:0')\n"
+        "inp = W.make_layer(W.CONFIGS[%r], %d, %r, seed=0, device='cuda:0')\n"
         "h = host_inputs(inp); sh = inp.shape\n"
         "ly = MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize, w_gu=inp.w_gu, w_down=inp.w_down, device='cuda:0')\n"
         "out = ly.forward(inp.x, inp.logits, ffn='gemm'); ly.check()\n"
-        "tok = sample_tokens(512)\n"
+        "tok = sample_tokens(%d)\n"
         "_, _, y = oracle_out(inp, h, tokens=tok)\n"
         "print(assert_close(to_np(out)[tok], y, 'bn'))\n"
     ) % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-         os.path.dirname(os.path.abspath(__file__)))
+         os.path.dirname(os.path.abspath(__file__)), case[0], case[1], case[2], case[1])
     env = dict(os.environ, MOE_GEMM_TILE=tile)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=600)
