@@ -310,11 +310,15 @@ moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, 
 //                or slower for bf16 once every stage took one copy per
 //                operand; int8 weights keep them for 8-48 rows, see
 //                pick_tile_w8.)
-//   more       : 128 x 256 tiles (0.75 of bf16 peak at 1024 rows per group).
+//   <= 128 rows: 128 x 256 tiles.
+//   more       : 256 x 256 tiles on CTA pairs (gemm_tc_pair.cu): 4-8 % faster
+//                than 128 x 256 for gate/up at 256-1024 rows per group and
+//                up to 6 % for down; at 64-128 rows they tie on gate/up and
+//                lose on down, so the pairs start above 128 rows.
 //                The 256-row token blocks of gemm_tc256.cu (a third fewer
-//                operand bytes per FLOP) measured 5-16 % slower at 32-1024
-//                rows per group once both kernels took one copy per operand
-//                per stage, so the choice never falls on them.
+//                operand bytes per FLOP) measured 5-16 % slower than 128 x 256
+//                at 32-1024 rows per group once both kernels took one copy per
+//                operand per stage, so the choice never falls on them.
 // MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill|pair in the environment
 // overrides the choice.
 static int forced_tile() {
@@ -336,7 +340,7 @@ static int forced_tile() {
 int pick_tile(int M, int G) {
     if (forced_tile() >= 0) return forced_tile();
     const int64_t m = M, g = G;
-    return m <= 64 * g ? TILE_128 : TILE_256;
+    return m <= 64 * g ? TILE_128 : m <= 128 * g ? TILE_256 : TILE_PAIR;
 }
 
 // int8 weights: the weight-row tiles for 8-48 rows per group (the 128-token
