@@ -10,9 +10,13 @@
 
 namespace moe {
 
-constexpr int CB_CPT = 2;             // 8-element chunks per thread
+// 8-element chunks per thread.  One keeps a thread within 64 registers with
+// its 8 row loads in flight, so an SM holds 1024 threads of them; two chunks
+// per thread (139 registers, 3 blocks per SM) left the batch's tokens to run
+// in ~5 waves and DRAM 43 % busy at T=2048.
+constexpr int CB_CPT = 1;
 
-__global__ void __launch_bounds__(256) combine_kernel(
+__global__ void __launch_bounds__(256, 4) combine_kernel(
     const uint16_t *__restrict__ y_perm, const int32_t *__restrict__ row_of_slot,
     const float *__restrict__ topk_w, const int32_t *__restrict__ offsets, int E, int T, int k,
     int S, int H, const uint16_t *residual, uint16_t *out, int32_t *dev_error) {
@@ -48,7 +52,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
     // every row's chunks, so the gathers overlap; sums stay in j order
     constexpr int BATCH = 8;
     for (int j0 = 0; j0 < k; j0 += BATCH) {
-        int64_t r[BATCH];
+        int32_t r[BATCH];
         float w[BATCH];
         bool ok[BATCH];
 #pragma unroll
@@ -68,7 +72,8 @@ __global__ void __launch_bounds__(256) combine_kernel(
         for (int j = 0; j < BATCH; ++j)
 #pragma unroll
             for (int q = 0; q < CB_CPT; ++q)
-                if (ok[j] && c0 + q < chunks) v[j][q] = ld_nc(y_perm + r[j] * H + (c0 + q) * 8);
+                if (ok[j] && c0 + q < chunks)
+                    v[j][q] = ld_nc(y_perm + static_cast<int64_t>(r[j]) * H + (c0 + q) * 8);
 #pragma unroll
         for (int j = 0; j < BATCH; ++j)
 #pragma unroll
@@ -130,7 +135,7 @@ static moe_status combine_impl(const uint16_t *y_perm, const int32_t *row_of_slo
     if (T > 65535) return MOE_ERR_UNSUPPORTED;   // grid.y limit
     const int chunks = H / 8;
     const int per_thread = (chunks + CB_CPT - 1) / CB_CPT;
-    const int threads = per_thread >= 128 ? 128 : ((per_thread + 31) / 32) * 32;
+    const int threads = per_thread >= 256 ? 256 : ((per_thread + 31) / 32) * 32;
     dim3 grid((per_thread + threads - 1) / threads, T);
     launch(combine_kernel, grid, threads, 0, stream, y_perm, row_of_slot, topk_w, offsets, E, T, k,
            S, H, residual, out, dev_error);
