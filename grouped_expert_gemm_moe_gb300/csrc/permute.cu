@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(1024) permute_place_kernel(
     __syncthreads();
     for (int g = threadIdx.x; g < E; g += blockDim.x) {
         int total = 0, before = 0;
+        // unrolled so that the chunks' counts are loaded together rather
+        // than one L2 round trip after another
+#pragma unroll 8
         for (int cc = 0; cc < nchunks; ++cc) {
             const int v = counts[static_cast<int64_t>(cc) * (E + 1) + g];
             total += v;
