@@ -92,28 +92,40 @@ def load_peaks():
                     source="fallback")
 
 
-def kernel_source_hash() -> str:
-    """Hash of every CUDA source: a committed traffic figure is used only
-    while the kernels it was measured on are unchanged."""
+# The CUDA sources behind each kernel named in a roofline object (with the
+# headers they include): a committed traffic figure is used only while these
+# are unchanged since the counters were taken.
+KERNEL_SOURCES = {
+    "tc_grouped_gemm_swiglu": ("gemm_tc.cu", "gemm_tc_pair.cu", "gemm_tc_dec.cu",
+                               "gemm_tc256.cu", "tc_common.cuh", "common.cuh"),
+    "decode_layer_kernel": ("decode_layer.cu", "gemv_tasks.cuh", "route_token.cuh",
+                            "common.cuh"),
+    "gemv_gateup_bf16": ("gemv.cu", "gemv_tasks.cuh", "common.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the CUDA sources of `kernel` (every source if it is not listed)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "grouped_expert_gemm_moe_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+    names = KERNEL_SOURCES.get(kernel) or sorted(
+        f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    for f in names:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
     """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[f"{kernel}@{workload}"]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
