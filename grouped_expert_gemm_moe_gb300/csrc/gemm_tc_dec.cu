@@ -54,7 +54,11 @@ struct DecCfg {
     // that L2 round trip into every k-step's hand-off.
     static constexpr int TOK_STAGES = KP == 2 ? (TN <= 32 ? 8 : 4) : (TN <= 32 ? 16 : 8);
     static constexpr int STAGES = W8 ? 4 : KP == 2 ? (TN <= 16 ? 5 : 4) : (TN <= 16 ? 10 : 8);
-    static constexpr int RAW_STAGES = W8 ? (TN <= 16 ? 12 : TN <= 32 ? 10 : 8) : 0;
+    static constexpr int RAW_STAGES = W8 ? (TN <= 16 ? 12 : 8) : 0;
+    // int8: converter groups take the k-steps in turn and wait by phase
+    // parity, so each stage of both rings must always fall to the same group
+    static_assert(!W8 || (STAGES % W8_GROUPS == 0 && RAW_STAGES % W8_GROUPS == 0),
+                  "each ring stage must belong to one converter group");
     static constexpr int XBUF_BYTES = 64 * TN * 4;              // up values, fp32
     static constexpr uint32_t TMEM_COLS = 2 * TN < 32 ? 32 : 2 * TN;
     static constexpr int BAR_BYTES = 1024;

@@ -26,7 +26,20 @@ namespace moe {
 constexpr int W8_BN = 256;
 constexpr int W8_STAGES = 3;        // activation + converted weight stages
 constexpr int W8_RAW = 4;           // raw int8 weight stages (the HBM stream)
-constexpr int W8_CONV_THREADS = 256;
+// Converter groups take the k-steps in turn (group = k-step mod
+// W8_CONV_GROUPS) and wait on barriers by phase parity, which cannot tell a
+// phase from the one two uses back: every barrier a converter waits on must
+// be waited on by one group only, in order.  The raw ring's depth is a
+// multiple of the group count for that; the stage-free signal of k-step q
+// goes to barrier q mod W8_FREE, W8_FREE a common multiple of the stage and
+// group counts, so the k-steps that wait on one barrier belong to one group.
+constexpr int W8_CONV_GROUPS = W8_GROUPS;
+constexpr int W8_FREE = 12;
+constexpr int W8_CONV_THREADS = W8_CONV_GROUPS * W8_GROUP_THREADS;
+static_assert(W8_RAW % W8_CONV_GROUPS == 0, "each raw stage must belong to one converter group");
+static_assert(W8_FREE % W8_STAGES == 0 && W8_FREE % W8_CONV_GROUPS == 0,
+              "stage-free barriers: a common multiple of stages and groups");
+static_assert((2 * W8_STAGES + W8_FREE + 2 * W8_RAW + 5) * 8 + 8 <= 512, "barrier block");
 constexpr int W8_THREADS = 7 * 32 + W8_CONV_THREADS;
 
 struct W8Cfg {
@@ -41,6 +54,15 @@ struct W8Cfg {
                2 * static_cast<size_t>(G + 1) * sizeof(int);
     }
 };
+
+// Wait until the stage k-step `seq` will use is free: k-step seq - S, the
+// stage's previous user, has been consumed by the MMA.
+__device__ __forceinline__ bool stage_free(uint64_t *ab_free, int seq, int32_t *dev_error) {
+    if (seq < W8_STAGES) return true;
+    const int q = seq - W8_STAGES;
+    return mbar_wait(&ab_free[q % W8_FREE], static_cast<uint32_t>((q / W8_FREE) & 1),
+                     dev_error);
+}
 
 // SWIGLU: out = h [M, NOUT=I], int8 weights [G*2I, K=H], scales [G*2I].
 // PLAIN : out = y [M, NOUT=H], int8 weights [G*H,  K=I], scales [G*H].
@@ -64,8 +86,8 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
     uint8_t *sQ = sB + S * C::B_BYTES;
     uint64_t *a_full = reinterpret_cast<uint64_t *>(sQ + RS * C::RAW_BYTES);
     uint64_t *b_full = a_full + S;
-    uint64_t *ab_empty = b_full + S;
-    uint64_t *q_full = ab_empty + S;
+    uint64_t *ab_empty = b_full + S;              // [W8_FREE], by k-step number
+    uint64_t *q_full = ab_empty + W8_FREE;
     uint64_t *q_empty = q_full + RS;
     uint64_t *accf = q_empty + RS;
     uint64_t *acce = accf + 2;
@@ -84,8 +106,8 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(&a_full[s], 1);
             mbar_init(&b_full[s], W8_GROUP_THREADS);
-            mbar_init(&ab_empty[s], 1);
         }
+        for (int i = 0; i < W8_FREE; ++i) mbar_init(&ab_empty[i], 1);
         for (int r = 0; r < RS; ++r) {
             mbar_init(&q_full[r], 1);
             mbar_init(&q_empty[r], W8_GROUP_THREADS);
@@ -118,7 +140,7 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
         // ------------------------------------------- activation producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
-            int s = 0;
+            int s = 0, seq = 0;
             uint32_t ph = 0, filled = 0, fill_par = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -132,7 +154,8 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
                                         : abox == 64 ? &tm_act64 : &tm_act128;
                 const uint32_t bytes = abox * TC_BK * 2;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&ab_empty[s], ph ^ 1u, dev_error)) { ok = false; break; }
+                    if (!stage_free(ab_empty, seq, dev_error)) { ok = false; break; }
+                    ++seq;
                     mbar_arrive_expect_tx(&a_full[s], bytes);
                     uint8_t *a = sA + s * C::A_BYTES;
                     tma_load_2d(a, tm_a, &a_full[s], kb * TC_BK, ti.m0, pol);
@@ -182,11 +205,11 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             for (int kb = 0; kb < KB; ++kb, ++seq) {
-                if (seq % W8_GROUPS != grp) continue;
+                if (seq % W8_CONV_GROUPS != grp) continue;
                 const int s = seq % S, r = seq % RS;
-                const uint32_t sph = (seq / S) & 1, rph = (seq / RS) & 1;
+                const uint32_t rph = (seq / RS) & 1;
                 if (!mbar_wait(&q_full[r], rph, dev_error) ||
-                    !mbar_wait(&ab_empty[s], sph ^ 1u, dev_error)) {
+                    !stage_free(ab_empty, seq, dev_error)) {
                     ok = false;
                     break;
                 }
@@ -200,7 +223,7 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
         // ------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
-            int s = 0, acc = 0;
+            int s = 0, acc = 0, seq = 0;
             uint32_t ph = 0, acc_ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -221,7 +244,8 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
                         tc_mma_bf16(d_tmem, sw128_kmajor_desc(a_addr + kk * 32),
                                     sw128_kmajor_desc(b_addr + kk * 32), idesc,
                                     (kb > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&ab_empty[s]);
+                    tc_commit(&ab_empty[seq % W8_FREE]);   // stage s is free after k-step seq
+                    ++seq;
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;

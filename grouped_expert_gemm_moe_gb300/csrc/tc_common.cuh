@@ -71,7 +71,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // The int8 converters work in W8_GROUPS independent groups of
-// W8_GROUP_THREADS threads; group c widens the k-steps c, c + W8_GROUPS, ...
+// W8_GROUP_THREADS threads (the token-row kernel of gemm_tc_w8.cu uses its
+// own group count); group c widens the k-steps c, c + W8_GROUPS, ...
 // of the CTA's sequence, so that several stages are converted at once and
 // the conversion latency (shared-memory round trips, the proxy fence, the
 // barrier hand-off) overlaps instead of adding up stage after stage.

@@ -182,3 +182,35 @@ def test_stack_graph_replay_matches_eager(mods):
         assert torch.equal(got, want), f"trial {trial}"
         g = torch.Generator(device=DEV).manual_seed(11 + trial)
         x0.copy_(torch.randn(x0.shape, generator=g, device=DEV).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "128"])
+def test_w8_gemm_tile_shapes_agree(tile):
+    """Every int8 tensor-core kernel, forced (weight-row tiles of 16/32/64
+    tokens, the 128-token-row kernel; normally chosen by rows per group),
+    matches the oracle's int8 layer on an OLMoE-shaped T=128 zipf batch
+    (group sizes from a few rows to several dozen)."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path.insert(0, %r); sys.path.insert(0, %r)\n"
+        "import torch, oracle\n"
+        "import __graft_entry__ as g; g.build()\n"
+        "from grouped_expert_gemm_moe_gb300 import binding as B, layer as L, workloads as W\n"
+        "import test_gpu_w8_stack as t\n"
+        "from gpu_helpers import assert_close, sample_tokens, to_np\n"
+        "layer, inp, (qg, sg, qd, sd) = t.w8_layer(B, L)\n"
+        "sh = W.OLMOE_W8\n"
+        "x, logits = t.batch(sh, 128, 'zipf', inp.w_r, 5)\n"
+        "out = layer.forward(x.to('cuda:0'), logits.to('cuda:0'), ffn='gemm'); layer.check()\n"
+        "tok = sample_tokens(128)\n"
+        "ids, w = oracle.route(logits.numpy(), sh.k, sh.renormalize)\n"
+        "y = oracle.moe_layer_w8(W.bf16_bits(x), ids, w, sh.E, sh.S, qg, sg, qd, sd, tokens=tok)\n"
+        "print(assert_close(to_np(out)[tok], y, 'w8 tile'))\n"
+    ) % (os.path.dirname(here), here)
+    env = dict(os.environ, MOE_GEMM_TILE=tile)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
