@@ -59,6 +59,7 @@ _SIGS = {
     "moe_quantize_w8": ([P, I64, I64, P, P], I),
     "moe_grouped_gemv_noalloc": ([P, P, I, I, I, I, P, P, P, P, P], I),
     "moe_route_permute": ([P, I, I, I, I, I, P, I, I, P, P, P, P, P, P, P, P], I),
+    "moe_copy": ([P, P, SZ, P], I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -419,3 +420,13 @@ def moe_quantize_w8(w: torch.Tensor):
     s = torch.empty(wc.shape[:-1], dtype=torch.float32)
     _ok(_lib.moe_quantize_w8(_ptr(wc), rows, K, _ptr(q), _ptr(s)), "moe_quantize_w8")
     return q, s
+
+
+def moe_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """dst <- src by the GPU's SMs (either may be pinned host memory)."""
+    if dst.nbytes != src.nbytes or not dst.is_contiguous() or not src.is_contiguous():
+        raise ValueError("moe_copy: contiguous tensors of the same size in bytes")
+    for t in (dst, src):
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("moe_copy: host tensors must be pinned")
+    _ok(_lib.moe_copy(_ptr(dst), _ptr(src), dst.nbytes, _stream(stream)), "moe_copy")

@@ -224,9 +224,62 @@ class MoELayer:
         logits hold.  Decode-sized batches are launch-bound without this."""
         return CapturedForward(self, x, logits, out, residual, ffn)
 
+    def capture_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, ffn="auto",
+                     residual=None) -> "CapturedHostForward":
+        """Like capture(), for inputs and output in pinned host memory: the
+        graph holds the copies of x and the logits to the device, the forward
+        pass and the copy of the output back, so a step is one graph launch.
+        replay() returns the pinned host output (valid after the stream is
+        synchronised); it reruns the step on whatever the host inputs hold."""
+        return CapturedHostForward(self, x_host, logits_host, ffn, residual)
+
     def check(self):
         """Synchronise and raise if any kernel reported a device-side fault."""
         B.check_device_error(self.err, "MoELayer")
+
+
+class CapturedHostForward:
+    """A forward pass with its host<->device copies recorded into one CUDA
+    graph (see MoELayer.capture_host)."""
+
+    def __init__(self, layer: MoELayer, x_host, logits_host, ffn, residual):
+        if x_host.is_cuda or logits_host.is_cuda:
+            raise ValueError("capture_host takes host tensors")
+        if not (x_host.is_pinned() and logits_host.is_pinned()):
+            raise ValueError("capture_host needs pinned host memory (tensor.pin_memory())")
+        self.layer, self.x_host, self.logits_host = layer, x_host, logits_host
+        dev = layer.device
+        self.x = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
+        self.logits = torch.empty(logits_host.shape, dtype=logits_host.dtype, device=dev)
+        T = x_host.shape[0]
+        self.out = torch.empty((T, layer.H), dtype=torch.bfloat16, device=dev)
+        self.out_host = torch.empty((T, layer.H), dtype=torch.bfloat16).pin_memory()
+
+        # the transfers are kernels of the library (moe_copy: SMs reading and
+        # writing the mapped pinned host memory over NVLink-C2C) when the
+        # sizes allow 16-byte copies, else copy-engine transfers
+        def transfer(dst, src):
+            if dst.nbytes % 16 == 0 and dst.data_ptr() % 16 == 0 and src.data_ptr() % 16 == 0:
+                B.moe_copy(dst, src)
+            else:
+                dst.copy_(src, non_blocking=True)
+
+        def step():
+            transfer(self.x, self.x_host)
+            transfer(self.logits, self.logits_host)
+            layer.forward(self.x, self.logits, out=self.out, residual=residual, ffn=ffn)
+            transfer(self.out_host, self.out)
+
+        step()                                  # eager pass: kernel attributes
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            step()
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
+        return self.out_host
 
 
 class CapturedForward:

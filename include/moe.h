@@ -350,6 +350,18 @@ moe_status moe_decode_layer(const float *logits, const uint16_t *x, int T, int E
                             size_t workspace_bytes, int32_t *dev_error, cudaStream_t stream);
 
 /*
+ * moe_copy -- copy `bytes` bytes from src to dst with the GPU's SMs (a
+ * grid-stride kernel of 16-byte loads and stores), for moving a layer's
+ * inputs in and its output out of pinned host memory: pinned host memory
+ * (cudaHostAlloc) is mapped into the device's address space, and on GB300
+ * the SMs reach it over NVLink-C2C.  Either pointer may be device memory or
+ * mapped pinned host memory; the regions must not overlap.  bytes must be a
+ * multiple of 16 and both pointers 16-byte aligned (else MOE_ERR_ALIGNMENT).
+ * Asynchronous on `stream`; may be captured into a CUDA graph.
+ */
+moe_status moe_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+
+/*
  * moe_quantize_w8 -- offline, host-side int8 quantisation of expert
  * weights ("dispatch" README, phase 5a: self-computed per-channel scales).
  * w_host: [rows, K] bf16 bits in host memory; q_host: [rows, K] int8 and

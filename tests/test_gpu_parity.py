@@ -441,3 +441,47 @@ def test_deepseek_16384_tokens(B, L):
                                   oracle.permute(ids, sh.E, sh.S)[0])
     y = oracle.moe_layer(h["x"], ids, w, sh.E, sh.S, h["w_gu"], h["w_down"], tokens=tok)
     assert_close(to_np(out)[tok], y, "DeepSeek T=16384")
+
+
+@pytest.mark.parametrize("name,T", [("olmoe", 64), ("olmoe", 1), ("deepseek", 512)])
+def test_capture_host_replays_match_forward(B, L, name, T):
+    """MoELayer.capture_host: the graph with the host<->device copies gives,
+    for each new content of the pinned host inputs, the same bytes as a
+    forward pass on device copies of them."""
+    sh = W.CONFIGS[name]
+    inp = W.make_layer(sh, T, "uniform", seed=2, device=DEV)
+    layer = L.MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize, w_gu=inp.w_gu,
+                       w_down=inp.w_down, device=DEV)
+    x_host = inp.x.cpu().pin_memory()
+    l_host = inp.logits.cpu().pin_memory()
+    cap = layer.capture_host(x_host, l_host)
+    with pytest.raises(ValueError):
+        layer.capture_host(inp.x.cpu(), inp.logits.cpu())      # not pinned
+    g = torch.Generator().manual_seed(T)
+    for _ in range(3):
+        x_host.copy_(torch.randn((T, sh.H), generator=g).to(torch.bfloat16))
+        l_host.copy_(torch.randn((T, sh.E), generator=g))
+        out = cap.replay()
+        torch.cuda.synchronize()
+        ref = layer.forward(x_host.to(DEV), l_host.to(DEV)).cpu()
+        layer.check()
+        assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096, 262144, 8 << 20])
+def test_moe_copy_both_directions(B, nbytes):
+    """moe_copy moves bytes exactly between pinned host memory and the device
+    (both directions) and device to device; sizes off the 16-byte grid are
+    refused."""
+    g = torch.Generator().manual_seed(nbytes)
+    src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g).pin_memory()
+    dev = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    B.moe_copy(dev, src)
+    dev2 = torch.zeros_like(dev)
+    B.moe_copy(dev2, dev)
+    B.moe_copy(back, dev2)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    with pytest.raises(B.MoEError):
+        B.moe_copy(dev[: nbytes - 1] if nbytes > 16 else dev[:8], src[: nbytes - 1] if nbytes > 16 else src[:8])
