@@ -98,6 +98,18 @@ def _dev(t: torch.Tensor, name: str, dtype=None):
     return t
 
 
+def _out(t: torch.Tensor, name: str, dtype=None):
+    """An output the kernels may write in device memory or in mapped pinned
+    host memory (stores over NVLink-C2C)."""
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
 def version() -> int:
     return int(_lib.moe_version())
 
@@ -350,7 +362,7 @@ def moe_grouped_gemv_w8(x_perm, offsets, q_gu, s_gu, q_down, s_down, y_perm, wor
 def moe_combine(y_perm, row_of_slot, topk_w, S, out, residual=None, dev_error=None,
                 stream=None):
     _dev(y_perm, "y_perm", torch.bfloat16); _dev(row_of_slot, "row_of_slot", torch.int32)
-    _dev(topk_w, "topk_w", torch.float32); _dev(out, "out", torch.bfloat16)
+    _dev(topk_w, "topk_w", torch.float32); _out(out, "out", torch.bfloat16)
     if residual is not None:
         _dev(residual, "residual", torch.bfloat16)
     T, k = topk_w.shape
@@ -365,7 +377,7 @@ def moe_combine_capped(y_perm, row_of_slot, topk_w, offsets, E, S, out, residual
     """moe_combine after moe_permute_capped (dropped slots add nothing; the
     shared rows start at offsets[E])."""
     _dev(y_perm, "y_perm", torch.bfloat16); _dev(row_of_slot, "row_of_slot", torch.int32)
-    _dev(topk_w, "topk_w", torch.float32); _dev(out, "out", torch.bfloat16)
+    _dev(topk_w, "topk_w", torch.float32); _out(out, "out", torch.bfloat16)
     _dev(offsets, "offsets", torch.int32)
     if residual is not None:
         _dev(residual, "residual", torch.bfloat16)
@@ -391,7 +403,7 @@ def moe_decode_layer(logits, x, k, renormalize, S, w_gu, w_down, out, workspace,
     grouped GEMV gate/up + down, combine); same bytes as the separate calls."""
     _dev(logits, "logits", torch.float32); _dev(x, "x", torch.bfloat16)
     _dev(w_gu, "w_gu", torch.bfloat16); _dev(w_down, "w_down", torch.bfloat16)
-    _dev(out, "out", torch.bfloat16); _dev(workspace, "workspace")
+    _out(out, "out", torch.bfloat16); _dev(workspace, "workspace")
     if residual is not None:
         _dev(residual, "residual", torch.bfloat16)
     if topk_ids is not None:

@@ -227,8 +227,9 @@ class MoELayer:
     def capture_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, ffn="auto",
                      residual=None) -> "CapturedHostForward":
         """Like capture(), for inputs and output in pinned host memory: the
-        graph holds the copies of x and the logits to the device, the forward
-        pass and the copy of the output back, so a step is one graph launch.
+        graph holds the copies of x and the logits to the device and the
+        forward pass, whose last kernel stores the output straight into a
+        pinned host buffer, so a step is one graph launch.
         replay() returns the pinned host output (valid after the stream is
         synchronised); it reruns the step on whatever the host inputs hold."""
         return CapturedHostForward(self, x_host, logits_host, ffn, residual)
@@ -252,7 +253,6 @@ class CapturedHostForward:
         self.x = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
         self.logits = torch.empty(logits_host.shape, dtype=logits_host.dtype, device=dev)
         T = x_host.shape[0]
-        self.out = torch.empty((T, layer.H), dtype=torch.bfloat16, device=dev)
         self.out_host = torch.empty((T, layer.H), dtype=torch.bfloat16).pin_memory()
 
         # the transfers are kernels of the library (moe_copy: SMs reading and
@@ -264,11 +264,13 @@ class CapturedHostForward:
             else:
                 dst.copy_(src, non_blocking=True)
 
+        # the layer's last kernel (combine, or the decode layer's combine
+        # phase) stores the output straight into the pinned host buffer, so
+        # the transfer back overlaps its own reads
         def step():
             transfer(self.x, self.x_host)
             transfer(self.logits, self.logits_host)
-            layer.forward(self.x, self.logits, out=self.out, residual=residual, ffn=ffn)
-            transfer(self.out_host, self.out)
+            layer.forward(self.x, self.logits, out=self.out_host, residual=residual, ffn=ffn)
 
         step()                                  # eager pass: kernel attributes
         torch.cuda.synchronize()

@@ -296,7 +296,9 @@ moe_status moe_grouped_gemv_noalloc(const uint16_t *x_perm, const int32_t *offse
  *                  + sum_{s<S} y_perm[T*k + s*T + t]  (+ residual[t]) )
  * summed in fp32 in that order.  y_perm: [M,H] bf16; row_of_slot: [T*k];
  * topk_w: [T,k] fp32; residual: [T,H] bf16 or NULL; out: [T,H] bf16 (may
- * alias residual).  A row index outside [0, T*k) is skipped.
+ * alias residual; device memory or mapped pinned host memory, which the
+ * kernel's stores reach over NVLink-C2C).  A row index outside [0, T*k) is
+ * skipped.
  */
 moe_status moe_combine(const uint16_t *y_perm, const int32_t *row_of_slot, const float *topk_w,
                        int T, int k, int S, int H, const uint16_t *residual, uint16_t *out,
@@ -335,7 +337,8 @@ size_t moe_decode_workspace_size(int T, int E, int S, int k, int H, int I);
  * moe_grouped_gemv -> moe_combine on the same inputs.
  * logits: [T,E] fp32; x: [T,H] bf16 (read by token, no gathered copy);
  * w_gu: [E+S,2I,H]; w_down: [E+S,H,I] bf16; residual: [T,H] bf16 or NULL;
- * out: [T,H] bf16 (may alias residual); topk_ids: [T,k] int32 and
+ * out: [T,H] bf16 (may alias residual; device memory or mapped pinned host
+ * memory, as for moe_combine); topk_ids: [T,k] int32 and
  * topk_w: [T,k] fp32 are written (NULL to skip).  workspace: at least
  * moe_decode_workspace_size bytes, 16-byte aligned, owned by the caller and
  * not shared with work in flight on another stream.
