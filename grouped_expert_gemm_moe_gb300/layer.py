@@ -227,9 +227,10 @@ class MoELayer:
     def capture_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, ffn="auto",
                      residual=None) -> "CapturedHostForward":
         """Like capture(), for inputs and output in pinned host memory: the
-        graph holds the copies of x and the logits to the device and the
-        forward pass, whose last kernel stores the output straight into a
-        pinned host buffer, so a step is one graph launch.
+        graph holds the copy of x to the device and the forward pass, whose
+        routing reads the logits from the host buffer and whose last kernel
+        stores the output straight into a pinned host buffer, so a step is
+        one graph launch.
         replay() returns the pinned host output (valid after the stream is
         synchronised); it reruns the step on whatever the host inputs hold."""
         return CapturedHostForward(self, x_host, logits_host, ffn, residual)
@@ -251,7 +252,6 @@ class CapturedHostForward:
         self.layer, self.x_host, self.logits_host = layer, x_host, logits_host
         dev = layer.device
         self.x = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
-        self.logits = torch.empty(logits_host.shape, dtype=logits_host.dtype, device=dev)
         T = x_host.shape[0]
         self.out_host = torch.empty((T, layer.H), dtype=torch.bfloat16).pin_memory()
 
@@ -267,10 +267,11 @@ class CapturedHostForward:
         # the layer's last kernel (combine, or the decode layer's combine
         # phase) stores the output straight into the pinned host buffer, so
         # the transfer back overlaps its own reads
+        # and the routing reads each logit once, straight from the host buffer
         def step():
             transfer(self.x, self.x_host)
-            transfer(self.logits, self.logits_host)
-            layer.forward(self.x, self.logits, out=self.out_host, residual=residual, ffn=ffn)
+            layer.forward(self.x, self.logits_host, out=self.out_host, residual=residual,
+                          ffn=ffn)
 
         step()                                  # eager pass: kernel attributes
         torch.cuda.synchronize()
