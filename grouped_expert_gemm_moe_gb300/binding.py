@@ -98,10 +98,11 @@ def _dev(t: torch.Tensor, name: str, dtype=None):
     return t
 
 
-def _out(t: torch.Tensor, name: str, dtype=None):
+def _dev_or_pinned(t: torch.Tensor, name: str, dtype=None):
     """A tensor the kernels may access in device memory or in mapped pinned
     host memory (loads and stores over NVLink-C2C): the logits read once by
-    the routing kernels, the output written once by the combine."""
+    the routing kernels, the output written once by the combine, the decode
+    layer's x."""
     if not t.is_cuda and not t.is_pinned():
         raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
     if not t.is_contiguous():
@@ -136,7 +137,7 @@ def moe_router_logits(x, w_r, bias, logits, stream=None):
     T, H = x.shape
     E = w_r.shape[0]
     _dev(x, "x", torch.bfloat16); _dev(w_r, "w_r", torch.bfloat16)
-    _out(logits, "logits", torch.float32)
+    _dev_or_pinned(logits, "logits", torch.float32)
     if bias is not None:
         _dev(bias, "bias", torch.float32)
     _ok(_lib.moe_router_logits(_ptr(x), _ptr(w_r), _ptr(bias), T, H, E, _ptr(logits),
@@ -152,7 +153,7 @@ def moe_router_route(x, w_r, bias, k, renormalize, topk_ids, topk_w, logits=None
     _dev(x, "x", torch.bfloat16); _dev(w_r, "w_r", torch.bfloat16)
     _dev(topk_ids, "topk_ids", torch.int32); _dev(topk_w, "topk_w", torch.float32)
     if logits is not None:
-        _out(logits, "logits", torch.float32)
+        _dev_or_pinned(logits, "logits", torch.float32)
     if bias is not None:
         _dev(bias, "bias", torch.float32)
     _ok(_lib.moe_router_route(_ptr(x), _ptr(w_r), _ptr(bias), T, H, E, k, int(renormalize),
@@ -161,7 +162,7 @@ def moe_router_route(x, w_r, bias, k, renormalize, topk_ids, topk_w, logits=None
 
 
 def moe_route(logits, k, renormalize, topk_ids, topk_w, dev_error=None, stream=None):
-    _out(logits, "logits", torch.float32)
+    _dev_or_pinned(logits, "logits", torch.float32)
     T, E = logits.shape
     _dev(topk_ids, "topk_ids", torch.int32); _dev(topk_w, "topk_w", torch.float32)
     _ok(_lib.moe_route(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(topk_ids),
@@ -235,7 +236,7 @@ ROUTE_PERMUTE_MAX_E = 256
 def moe_route_permute(logits, k, renormalize, S, x, topk_ids, topk_w, offsets, sorted_slot,
                       row_of_slot, x_perm, dev_error=None, stream=None):
     """moe_route + moe_permute in one launch (T*k <= 1024, E <= 256)."""
-    _out(logits, "logits", torch.float32)
+    _dev_or_pinned(logits, "logits", torch.float32)
     T, E = logits.shape
     _dev(x, "x")
     if x.dtype == torch.bfloat16:
@@ -363,7 +364,7 @@ def moe_grouped_gemv_w8(x_perm, offsets, q_gu, s_gu, q_down, s_down, y_perm, wor
 def moe_combine(y_perm, row_of_slot, topk_w, S, out, residual=None, dev_error=None,
                 stream=None):
     _dev(y_perm, "y_perm", torch.bfloat16); _dev(row_of_slot, "row_of_slot", torch.int32)
-    _dev(topk_w, "topk_w", torch.float32); _out(out, "out", torch.bfloat16)
+    _dev(topk_w, "topk_w", torch.float32); _dev_or_pinned(out, "out", torch.bfloat16)
     if residual is not None:
         _dev(residual, "residual", torch.bfloat16)
     T, k = topk_w.shape
@@ -378,7 +379,7 @@ def moe_combine_capped(y_perm, row_of_slot, topk_w, offsets, E, S, out, residual
     """moe_combine after moe_permute_capped (dropped slots add nothing; the
     shared rows start at offsets[E])."""
     _dev(y_perm, "y_perm", torch.bfloat16); _dev(row_of_slot, "row_of_slot", torch.int32)
-    _dev(topk_w, "topk_w", torch.float32); _out(out, "out", torch.bfloat16)
+    _dev(topk_w, "topk_w", torch.float32); _dev_or_pinned(out, "out", torch.bfloat16)
     _dev(offsets, "offsets", torch.int32)
     if residual is not None:
         _dev(residual, "residual", torch.bfloat16)
@@ -402,9 +403,9 @@ def moe_decode_layer(logits, x, k, renormalize, S, w_gu, w_down, out, workspace,
                      topk_ids=None, topk_w=None, dev_error=None, stream=None):
     """The whole layer for T <= 8 tokens in one cooperative launch (route,
     grouped GEMV gate/up + down, combine); same bytes as the separate calls."""
-    _out(logits, "logits", torch.float32); _dev(x, "x", torch.bfloat16)
+    _dev_or_pinned(logits, "logits", torch.float32); _dev_or_pinned(x, "x", torch.bfloat16)
     _dev(w_gu, "w_gu", torch.bfloat16); _dev(w_down, "w_down", torch.bfloat16)
-    _out(out, "out", torch.bfloat16); _dev(workspace, "workspace")
+    _dev_or_pinned(out, "out", torch.bfloat16); _dev(workspace, "workspace")
     if residual is not None:
         _dev(residual, "residual", torch.bfloat16)
     if topk_ids is not None:

@@ -264,14 +264,23 @@ class CapturedHostForward:
             else:
                 dst.copy_(src, non_blocking=True)
 
-        # the layer's last kernel (combine, or the decode layer's combine
+        # The layer's last kernel (combine, or the decode layer's combine
         # phase) stores the output straight into the pinned host buffer, so
-        # the transfer back overlaps its own reads
-        # and the routing reads each logit once, straight from the host buffer
+        # the transfer back overlaps its own reads, and the routing reads the
+        # logits straight from their host buffer.  x: the single-launch decode
+        # layer reads it from the host buffer too (measured 4 us cheaper than
+        # copying it at T=1); the permute's gather does not (measured 4 us
+        # slower at T=64 and 260 us slower at T=2048), so x is copied there.
+        kind = layer.choose_path(T, x_host.dtype) if ffn == "auto" else ffn
+
         def step():
+            if kind == "decode":
+                layer.forward(self.x_host, self.logits_host, out=self.out_host,
+                              residual=residual, ffn=kind)
+                return
             transfer(self.x, self.x_host)
             layer.forward(self.x, self.logits_host, out=self.out_host, residual=residual,
-                          ffn=ffn)
+                          ffn=kind)
 
         step()                                  # eager pass: kernel attributes
         torch.cuda.synchronize()

@@ -21,9 +21,9 @@
  *    G = E + S expert groups, M = T*k + S*T permuted rows.  Slot s = t*k + j
  *    is token t's j-th routed choice.
  *  - Pointers are plain device pointers unless a parameter says "host".
- *    The routing calls' logits and the combine calls' out may also be
- *    mapped pinned host memory (cudaHostAlloc): the kernels read or write
- *    each element of them once, over NVLink-C2C on GB300.
+ *    The routing calls' logits, the combine calls' out and
+ *    moe_decode_layer's logits, x and out may also be mapped pinned host
+ *    memory (cudaHostAlloc), reached over NVLink-C2C on GB300.
  *    The caller owns every buffer: the library never allocates device
  *    memory, never synchronises, and enqueues all device work on `stream`
  *    (asynchronous to the host).  bf16 tensors are passed as uint16_t bit
