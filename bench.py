@@ -554,6 +554,26 @@ def run_oracle_tokens(inp, host, tokens, wbits, nthreads=0):
                             nthreads=nthreads)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(inp, gpu_out, min_seconds=10.0, min_seconds_1_thread=2.0):
     """The oracle, as it stands, on the host cores: route + permute + layer
     of every token of the batch, repeated until at least min_seconds of
@@ -590,6 +610,7 @@ def cpu_baseline(inp, gpu_out, min_seconds=10.0, min_seconds_1_thread=2.0):
         sec1 += time.perf_counter() - t0
         reps1 += 1
     return dict(value=round(reps * len(tokens) / sec, 3), unit=UNIT, cores=cores, kind="oracle",
+                cpu=cpu_model(),
                 sample=f"route+permute+layer of all {len(tokens)} tokens of the timed batch, "
                        f"{reps} times ({sec:.1f} s)",
                 value_1_thread=round(reps1 * len(t1) / sec1, 3),
@@ -700,7 +721,7 @@ def run_ours(args):
         }
         if base is not None:
             line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind",
-                                                         "sample", "value_1_thread",
+                                                         "cpu", "sample", "value_1_thread",
                                                          "sample_1_thread")}
             line["parity_vs_oracle"] = base["parity"]
         print(json.dumps(line), flush=True)
