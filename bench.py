@@ -766,6 +766,7 @@ def run_reference(args):
         "config": {"workload": args.workload, "layer": shape.name, "T": T, "H": shape.H,
                    "E": shape.E, "k": shape.k, "I": shape.I, "S": shape.S, "routing": routing},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": per, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"per step: route+permute+layer of {per} of the {T} tokens"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
