@@ -319,8 +319,8 @@ moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, 
 //                operand bytes per FLOP) measured 5-16 % slower than 128 x 256
 //                at 32-1024 rows per group once both kernels took one copy per
 //                operand per stage, so the choice never falls on them.
-// MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill|pair in the environment
-// overrides the choice.
+// MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill|pair (and, int8 only,
+// w8d16|w8d32) in the environment overrides the choice.
 static int forced_tile() {
     static const int forced = [] {
         const char *v = getenv("MOE_GEMM_TILE");
@@ -332,6 +332,8 @@ static int forced_tile() {
         if (!strcmp(v, "256")) return static_cast<int>(TILE_256);
         if (!strcmp(v, "prefill")) return static_cast<int>(TILE_PREFILL);
         if (!strcmp(v, "pair")) return static_cast<int>(TILE_PAIR);
+        if (!strcmp(v, "w8d16")) return static_cast<int>(TILE_W8D16);
+        if (!strcmp(v, "w8d32")) return static_cast<int>(TILE_W8D32);
         return -1;
     }();
     return forced;
@@ -343,15 +345,22 @@ int pick_tile(int M, int G) {
     return m <= 64 * g ? TILE_128 : m <= 128 * g ? TILE_256 : TILE_PAIR;
 }
 
-// int8 weights: the weight-row tiles up to 48 rows per group (the 128-token
-// int8 kernel widens 256 weight rows per k-step for a handful of tokens;
-// with 16-token tiles the OLMoE int8 layer measured 127.5 against 138.1 us
-// at T=8 and 168.4 against 173.0 us at T=64).
+// int8 weights, from the mean rows per group (OLMoE int8 layer on GB300, us
+// per layer; 256-row weight tiles of gemm_tc_dec_w8.cu with 16/32 tokens,
+// 128-row weight tiles of gemm_tc_dec.cu with 64 tokens, 256-token-row
+// tiles):
+//     rows/group      1      2      8     16     24     32     48     64
+//     w8d16        99.3  119.8  123.4  162.7  188.9  231.9  295.9  383.5
+//     w8d32       105.0  125.4  127.5  127.9  132.0  173.3  197.1  242.2
+//     dec64       131.7  170.5  173.3  174.6  179.1  180.7  180.8  244.3
+//     256         139.8  170.9  174.6  175.3  179.1  180.9  184.8  190.9
+// (the 128-row tiles with 16 and 32 tokens: 127.5 / 129.5 us at 1 row per
+// group, 168.7 / 170.5 at 8.)
 int pick_tile_w8(int M, int G) {
     if (forced_tile() >= 0) return forced_tile();
     const int64_t m = M, g = G;
-    if (m <= 10 * g) return TILE_DEC16;
-    if (m <= 20 * g) return TILE_DEC32;
+    if (m <= 10 * g) return TILE_W8D16;
+    if (m <= 36 * g) return TILE_W8D32;
     if (m <= 48 * g) return TILE_DEC64;
     return TILE_256;
 }

@@ -184,10 +184,11 @@ def test_stack_graph_replay_matches_eager(mods):
         x0.copy_(torch.randn(x0.shape, generator=g, device=DEV).to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "128"])
+@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "w8d16", "w8d32", "128"])
 def test_w8_gemm_tile_shapes_agree(tile):
-    """Every int8 tensor-core kernel, forced (weight-row tiles of 16/32/64
-    tokens, the 128-token-row kernel; normally chosen by rows per group),
+    """Every int8 tensor-core kernel, forced (128-row weight tiles of 16/32/64
+    tokens, 256-row weight tiles of 16/32 tokens, the 128-token-row kernel;
+    normally chosen by rows per group),
     matches the oracle's int8 layer on an OLMoE-shaped T=128 zipf batch
     (group sizes from a few rows to several dozen)."""
     import os
@@ -214,3 +215,20 @@ def test_w8_gemm_tile_shapes_agree(tile):
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("tile", ["w8d16", "w8d32", "dec16"])
+def test_w8_forced_tiles_on_ragged_shapes(tile):
+    """The ragged-tile rows test (K not a multiple of 64, intermediate and
+    hidden sizes that leave partial 128- and 256-row weight tiles, 12 to
+    1000 tokens) with one int8 weight-row kernel forced for every call."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, MOE_GEMM_TILE=tile)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu",
+                        os.path.join(here, "test_gpu_w8_stack.py"), "-k", "rows_vs_oracle"],
+                       env=env, capture_output=True, text=True, timeout=900,
+                       cwd=os.path.dirname(here))
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
