@@ -193,6 +193,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     }
 }
 
+// The same wait with one outcome for the whole warp (every lane calls it):
+// the warp-collective tcgen05.ld / tcgen05.st after it need every lane, even
+// when the time limit runs out in some lanes only.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
+                                               int32_t *dev_error) {
+    return __all_sync(FULL, mbar_wait(bar, parity, dev_error));
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const TileInfo ti = decode_tile(t, s_tile, s_off, G);
-            if (!mbar_wait(&accf[acc], acc_phase, dev_error)) break;
+            if (!mbar_wait_warp(&accf[acc], acc_phase, dev_error)) break;
             tc_fence_after();
             const bool valid = row_in_tile < ti.nrows;
             uint16_t *orow = out + static_cast<int64_t>(ti.m0 + row_in_tile) * NOUT;

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const PTile ti = p_decode(t, s_tile, s_off, G);
-            if (!mbar_wait(accf, acc_phase, dev_error)) break;
+            if (!mbar_wait_warp(accf, acc_phase, dev_error)) break;
             tc_fence_after();
             if (half == 0 || ti.two) {
                 const bool valid = row_in_tile < ti.rows;

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(DecCfg<W8, TN, KP>::THREADS, 1)
         uint32_t acc_ph = 0, x_ph = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const TileInfo ti = decode_tile(t, s_tile, s_off, G, TN);
-            if (!mbar_wait(&accf[acc], acc_ph, dev_error)) break;
+            if (!mbar_wait_warp(&accf[acc], acc_ph, dev_error)) break;
             tc_fence_after();
             float d[TN];
             {
@@ -319,12 +319,12 @@ __global__ void __launch_bounds__(DecCfg<W8, TN, KP>::THREADS, 1)
                 if (W8 && i < NOUT)
                     sc = scales[static_cast<int64_t>(ti.g) * R + (up ? UP_OFF : 0) + i];
                 if (up) {
-                    if (!mbar_wait(x_empty, x_ph ^ 1u, dev_error)) break;
+                    if (!mbar_wait_warp(x_empty, x_ph ^ 1u, dev_error)) break;
 #pragma unroll
                     for (int j = 0; j < TN; ++j) xbuf[j * 64 + (f - 64)] = d[j] * sc;
                     mbar_arrive(x_full);
                 } else {
-                    if (!mbar_wait(x_full, x_ph, dev_error)) break;
+                    if (!mbar_wait_warp(x_full, x_ph, dev_error)) break;
                     if (i < NOUT) {
                         uint16_t *col = out + static_cast<int64_t>(ti.m0) * NOUT + i;
 #pragma unroll

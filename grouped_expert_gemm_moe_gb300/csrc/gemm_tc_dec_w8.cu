@@ -131,14 +131,6 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// A barrier wait with the same outcome in every lane of the warp: the
-// warp-collective tcgen05 instructions after it need the whole warp, even
-// when the time limit runs out for some lanes only.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
-                                               int32_t *dev_error) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, dev_error));
-}
-
 }  // namespace
 
 // SWIGLU: out = h [M, NOUT=I], int8 weights [G*2I, K=H] (up rows at +UP_OFF = I).

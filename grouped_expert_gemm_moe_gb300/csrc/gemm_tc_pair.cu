@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint32_t acc_phase = 0;
         for (int t = t_first; t < total; t += t_step) {
             const TileInfo ti = decode_tile(t, s_tile, s_off, G, PAIR_BM);
-            if (!mbar_wait(&accf[acc], acc_phase, dev_error)) break;
+            if (!mbar_wait_warp(&accf[acc], acc_phase, dev_error)) break;
             tc_fence_after();
             // Accumulator layout (per CTA, TMEM columns from tbase):
             //   M = 256 tile: lane i = row i, columns 0..255 = the tile's 256
