@@ -97,7 +97,7 @@ def load_peaks():
 # are unchanged since the counters were taken.
 KERNEL_SOURCES = {
     "tc_grouped_gemm_swiglu": ("gemm_tc.cu", "gemm_tc_pair.cu", "gemm_tc_dec.cu",
-                               "gemm_tc256.cu", "tc_common.cuh", "common.cuh"),
+                               "gemm_tc256.cu", "tc_common.cuh", "tc_pair.cuh", "common.cuh"),
     "decode_layer_kernel": ("decode_layer.cu", "gemv_tasks.cuh", "route_token.cuh",
                             "common.cuh"),
     "gemv_gateup_bf16": ("gemv.cu", "gemv_tasks.cuh", "common.cuh"),

@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(DecCfg<W8, TN, KP>::THREADS, 1)
                     ok = false;
                     break;
                 }
+                // the stage's last reader was the tensor core (async proxy):
+                // order its reads before these generic writes
+                fence_proxy_async_smem();
                 widen_stage<DEC_BM>(sQ + r * C::RAW_BYTES, sA + s * C::A_BYTES, gt);
                 fence_proxy_async_smem();     // generic-proxy writes -> visible to the MMA
                 mbar_arrive(&a_full[s]);

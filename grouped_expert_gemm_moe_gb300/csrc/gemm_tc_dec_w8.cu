@@ -48,6 +48,7 @@
 // frees TMEM and returns; waits followed by warp-collective tcgen05
 // instructions take the same outcome in every lane.
 #include "tc_common.cuh"
+#include "tc_w8.cuh"
 
 namespace moe {
 
@@ -288,8 +289,9 @@ __global__ void __launch_bounds__(DwCfg<TN, NG, KP, GW>::THREADS, 1)
                 for (int p = 0; p < 4 * KPT; ++p)
                     v[p] = *reinterpret_cast<const uint4 *>(row + (p >> 2) * DW_KBLK_BYTES +
                                                             (((p & 3) ^ rsw) << 4));
+                const uint32_t done = loads_done(v);   // 0, once the loads have landed
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&q_empty[r]);   // the warp's rows are in registers
+                if (lane == 0) mbar_arrive(&q_empty[r + done]);   // the warp's rows are in registers
                 if (!mbar_wait_warp(&a_empty[s], sph ^ 1u, dev_error)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -441,25 +443,6 @@ __global__ void __launch_bounds__(DwCfg<TN, NG, KP, GW>::THREADS, 1)
 
 // ------------------------------------------------------------------ host
 
-namespace {
-
-// int8 tensor maps with the 64-byte swizzle (box rows of 64 bytes).
-// SwiGLU: the gate/up weights [G, 2, I, K] as {K, I, 2G}, box {64, 128, 2};
-// PLAIN: [rows, K] as {K, rows}, box {64, 256}.
-bool encode_u8_sw64(CUtensorMap *map, const void *base, uint64_t K, uint64_t I, uint64_t G2,
-                    bool three_d, uint32_t box_rows) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {K, I, G2};
-    const cuuint64_t strides[2] = {K, I * K};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(TC_BK), box_rows, 2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, three_d ? 3 : 2, const_cast<void *>(base), dims,
-               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
 
 template <bool SWIGLU, int TN, int NG, int KP, int GW>
 static moe_status launch_dw(const void *tok, const void *q, const float *scales,

@@ -213,6 +213,9 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
                     ok = false;
                     break;
                 }
+                // the stage's last reader was the tensor core (async proxy):
+                // order its reads before these generic writes
+                fence_proxy_async_smem();
                 widen_stage<BN>(sQ + r * C::RAW_BYTES, sB + s * C::B_BYTES, gt);
                 fence_proxy_async_smem();     // generic-proxy writes -> visible to the MMA
                 mbar_arrive(&b_full[s]);

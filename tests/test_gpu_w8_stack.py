@@ -221,7 +221,7 @@ def test_w8_gemm_tile_shapes_agree(tile):
 def test_w8_forced_tiles_on_ragged_shapes(tile):
     """The ragged-tile rows test (K not a multiple of 64, intermediate and
     hidden sizes that leave partial 128- and 256-row weight tiles, 12 to
-    1000 tokens) with one int8 weight-row kernel forced for every call."""
+    1000 tokens) with one int8 tile kernel forced for every call."""
     import os
     import subprocess
     import sys
