@@ -320,7 +320,7 @@ moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, 
 //                at 32-1024 rows per group once both kernels took one copy per
 //                operand per stage, so the choice never falls on them.
 // MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill|pair (and, int8 only,
-// w8d16|w8d32) in the environment overrides the choice.
+// w8d16|w8d32|w8d64) in the environment overrides the choice.
 static int forced_tile() {
     static const int forced = [] {
         const char *v = getenv("MOE_GEMM_TILE");
@@ -334,6 +334,7 @@ static int forced_tile() {
         if (!strcmp(v, "pair")) return static_cast<int>(TILE_PAIR);
         if (!strcmp(v, "w8d16")) return static_cast<int>(TILE_W8D16);
         if (!strcmp(v, "w8d32")) return static_cast<int>(TILE_W8D32);
+        if (!strcmp(v, "w8d64")) return static_cast<int>(TILE_W8D64);
         return -1;
     }();
     return forced;
@@ -346,22 +347,27 @@ int pick_tile(int M, int G) {
 }
 
 // int8 weights, from the mean rows per group (OLMoE int8 layer on GB300, us
-// per layer; 256-row weight tiles of gemm_tc_dec_w8.cu with 16/32 tokens,
+// per layer; 256-row weight tiles of gemm_tc_dec_w8.cu with 16/32/64 tokens,
 // 128-row weight tiles of gemm_tc_dec.cu with 64 tokens, 256-token-row
 // tiles):
 //     rows/group      1      2      8     16     24     32     48     64
 //     w8d16        99.3  119.8  123.4  162.7  188.9  231.9  295.9  383.5
 //     w8d32       105.0  125.4  127.5  127.9  132.0  173.3  197.1  242.2
+//     w8d64                                          137.7  145.9  162.8
 //     dec64       131.7  170.5  173.3  174.6  179.1  180.7  180.8  244.3
 //     256         139.8  170.9  174.6  175.3  179.1  180.9  184.8  190.9
+//     rows/group     96    128    192    256
+//     w8d64       215.5  260.6  346.6  439.2
+//     256         201.7  242.2  324.5  399.8
 // (the 128-row tiles with 16 and 32 tokens: 127.5 / 129.5 us at 1 row per
-// group, 168.7 / 170.5 at 8.)
+// group, 168.7 / 170.5 at 8; 256-row tiles with 128 tokens and a single
+// accumulator buffer: 207 us at 64 rows, 428 at 256.)
 int pick_tile_w8(int M, int G) {
     if (forced_tile() >= 0) return forced_tile();
     const int64_t m = M, g = G;
     if (m <= 10 * g) return TILE_W8D16;
-    if (m <= 36 * g) return TILE_W8D32;
-    if (m <= 48 * g) return TILE_DEC64;
+    if (m <= 24 * g) return TILE_W8D32;
+    if (m <= 64 * g) return TILE_W8D64;
     return TILE_256;
 }
 }  // namespace moe

@@ -465,7 +465,7 @@ static moe_status launch_dw(const void *tok, const void *q, const float *scales,
     return launch_status();
 }
 
-// Token-block height TN (16 or 32) for the 256-row int8 weight tiles.
+// Token-block height TN (16, 32 or 64) for the 256-row int8 weight tiles.
 template <bool SWIGLU>
 moe_status launch_dec_w8(int tn, const void *tok, const void *q, const float *scales,
                          const int32_t *offsets, int G, int M, int K, int R, int NOUT, int UP_OFF,
@@ -473,7 +473,10 @@ moe_status launch_dec_w8(int tn, const void *tok, const void *q, const float *sc
     if (tn == 16)
         return launch_dw<SWIGLU, 16, DW_NG, DW_KP, DW_GW>(tok, q, scales, offsets, G, M, K, R, NOUT,
                                                           UP_OFF, out, dev_error, stream);
-    return launch_dw<SWIGLU, 32, DW_NG, DW_KP, DW_GW>(tok, q, scales, offsets, G, M, K, R, NOUT,
+    if (tn == 32)
+        return launch_dw<SWIGLU, 32, DW_NG, DW_KP, DW_GW>(tok, q, scales, offsets, G, M, K, R,
+                                                          NOUT, UP_OFF, out, dev_error, stream);
+    return launch_dw<SWIGLU, 64, DW_NG, DW_KP, DW_GW>(tok, q, scales, offsets, G, M, K, R, NOUT,
                                                       UP_OFF, out, dev_error, stream);
 }
 

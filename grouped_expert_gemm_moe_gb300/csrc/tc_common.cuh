@@ -242,7 +242,7 @@ inline bool raise_smem_limit(Kernel kernel, int *done_per_device) {
 // Tile shapes of the grouped GEMMs (gemm_tc.cu picks one per call).
 enum {
     TILE_DEC16 = 0, TILE_DEC32, TILE_DEC64, TILE_128, TILE_256, TILE_PREFILL, TILE_PAIR,
-    TILE_W8D16, TILE_W8D32
+    TILE_W8D16, TILE_W8D32, TILE_W8D64
 };
 int pick_tile(int M, int G);
 int pick_tile_w8(int M, int G);
@@ -254,7 +254,7 @@ moe_status launch_dec(int tn, const void *tok, const void *w, const float *scale
                       const int32_t *offsets, int G, int M, int K, int R, int NOUT, int UP_OFF,
                       uint16_t *out, int32_t *dev_error, cudaStream_t stream);
 
-// int8 weights, 256 weight rows x TN (16 or 32) token rows (gemm_tc_dec_w8.cu).
+// int8 weights, 256 weight rows x TN (16, 32 or 64) token rows (gemm_tc_dec_w8.cu).
 template <bool SWIGLU>
 moe_status launch_dec_w8(int tn, const void *tok, const void *q, const float *scales,
                          const int32_t *offsets, int G, int M, int K, int R, int NOUT, int UP_OFF,

@@ -184,10 +184,10 @@ def test_stack_graph_replay_matches_eager(mods):
         x0.copy_(torch.randn(x0.shape, generator=g, device=DEV).to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "w8d16", "w8d32", "128"])
+@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "w8d16", "w8d32", "w8d64", "128"])
 def test_w8_gemm_tile_shapes_agree(tile):
     """Every int8 tensor-core kernel, forced (128-row weight tiles of 16/32/64
-    tokens, 256-row weight tiles of 16/32 tokens, the 128-token-row kernel;
+    tokens, 256-row weight tiles of 16/32/64 tokens, the 128-token-row kernel;
     normally chosen by rows per group),
     matches the oracle's int8 layer on an OLMoE-shaped T=128 zipf batch
     (group sizes from a few rows to several dozen)."""
@@ -217,7 +217,7 @@ def test_w8_gemm_tile_shapes_agree(tile):
     assert r.returncode == 0, r.stdout + r.stderr
 
 
-@pytest.mark.parametrize("tile", ["w8d16", "w8d32", "dec16"])
+@pytest.mark.parametrize("tile", ["w8d16", "w8d32", "w8d64", "dec16"])
 def test_w8_forced_tiles_on_ragged_shapes(tile):
     """The ragged-tile rows test (K not a multiple of 64, intermediate and
     hidden sizes that leave partial 128- and 256-row weight tiles, 12 to
