@@ -7,15 +7,17 @@
 //
 //   warp 0      TMA producer of the activation tiles (bf16, 128-byte swizzle)
 //   warp 6      TMA producer of the raw int8 weight tiles (own 4-deep ring)
-//   warps 7-14  converters, four groups taking turns by k-step: int8 -> bf16
-//               (exact: |q| <= 127 has 8 significant bits) into the
-//               128-byte-swizzled K-major layout the MMA reads
+//   warps 7-14  converters, four groups taking turns by k-step: each thread
+//               reads its 16-byte chunks of the raw tile into registers,
+//               releases the raw stage, waits for a free converted stage and
+//               widens int8 -> bf16 (exact: |q| <= 127 has 8 significant
+//               bits) into the 128-byte-swizzled K-major layout the MMA reads
 //   warp 1      TMEM allocator + MMA issuer (M = 128 tokens, N = 256 weights)
-//
-// Decode-sized groups go to the weight-row tiles of gemm_tc_dec.cu instead
-// (same widening, with the MMA's 128 rows spent on weight rows).
 //   warps 2-5   epilogue: accumulator * per-row scale (= sum x*q*scale, the
 //               dequantised product), then SwiGLU or a plain bf16 store.
+//
+// Groups of up to 56 rows go to the 256-row weight tiles of gemm_tc_dec_w8.cu
+// instead (the weights as the MMA's M, widened into tensor memory).
 //
 // The tile scheduler, tile order and failure handling (bounded waits, drains,
 // TMEM freed on every path) are those of the bf16 kernel in gemm_tc.cu.
