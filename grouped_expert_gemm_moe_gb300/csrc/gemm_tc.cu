@@ -352,12 +352,13 @@ int pick_tile(int M, int G) {
 // tiles of gemm_tc_w8.cu):
 //     rows/group      1      2      8     16     24     32     48     64
 //     w8d16        99.3  119.8  123.4  162.7  188.9  231.9  295.9  383.5
-//     w8d32       105.0  125.4  127.5  127.9  132.0  174.6  195.1  240.1
-//     w8d64                                   136.1  137.7  141.6  163.0
+//     w8d32       105.0  125.4  127.5  127.9  132.0  173.3  197.1  242.2
+//     w8d64                                          137.7  145.9  162.8
 //     dec64       131.7  170.5  173.3  174.6  179.1  180.7  180.8  244.3
-//     256         139.8  170.9  174.6  175.3  150.4  152.0  154.1  160.8
-//     rows/group     96    128    256
-//     256         173.0  205.3  332.5
+//     256         139.8  170.9  174.6  175.3  179.1  180.9  184.8  190.9
+//     rows/group     96    128    192    256
+//     w8d64       215.5  260.6  346.6  439.2
+//     256         201.7  242.2  324.5  399.8
 // (the 128-row tiles with 16 and 32 tokens: 127.5 / 129.5 us at 1 row per
 // group, 168.7 / 170.5 at 8; 256-row tiles with 128 tokens and a single
 // accumulator buffer: 207 us at 64 rows, 428 at 256.)
@@ -366,7 +367,7 @@ int pick_tile_w8(int M, int G) {
     const int64_t m = M, g = G;
     if (m <= 10 * g) return TILE_W8D16;
     if (m <= 24 * g) return TILE_W8D32;
-    if (m <= 56 * g) return TILE_W8D64;
+    if (m <= 64 * g) return TILE_W8D64;
     return TILE_256;
 }
 }  // namespace moe

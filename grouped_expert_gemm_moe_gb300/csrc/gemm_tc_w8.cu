@@ -7,22 +7,20 @@
 //
 //   warp 0      TMA producer of the activation tiles (bf16, 128-byte swizzle)
 //   warp 6      TMA producer of the raw int8 weight tiles (own 4-deep ring)
-//   warps 7-14  converters, four groups taking turns by k-step: each thread
-//               reads its 16-byte chunks of the raw tile into registers,
-//               releases the raw stage, waits for a free converted stage and
-//               widens int8 -> bf16 (exact: |q| <= 127 has 8 significant
-//               bits) into the 128-byte-swizzled K-major layout the MMA reads
+//   warps 7-14  converters, four groups taking turns by k-step: int8 -> bf16
+//               (exact: |q| <= 127 has 8 significant bits) into the
+//               128-byte-swizzled K-major layout the MMA reads
 //   warp 1      TMEM allocator + MMA issuer (M = 128 tokens, N = 256 weights)
+//
 //   warps 2-5   epilogue: accumulator * per-row scale (= sum x*q*scale, the
 //               dequantised product), then SwiGLU or a plain bf16 store.
 //
-// Groups of up to 56 rows go to the 256-row weight tiles of gemm_tc_dec_w8.cu
+// Groups of up to 64 rows go to the 256-row weight tiles of gemm_tc_dec_w8.cu
 // instead (the weights as the MMA's M, widened into tensor memory).
 //
 // The tile scheduler, tile order and failure handling (bounded waits, drains,
 // TMEM freed on every path) are those of the bf16 kernel in gemm_tc.cu.
 #include "tc_common.cuh"
-#include "tc_w8.cuh"
 
 namespace moe {
 
@@ -211,34 +209,18 @@ __global__ void __launch_bounds__(W8_THREADS, 1)
                 if (seq % W8_CONV_GROUPS != grp) continue;
                 const int s = seq % S, r = seq % RS;
                 const uint32_t rph = (seq / RS) & 1;
-                if (!mbar_wait(&q_full[r], rph, dev_error)) { ok = false; break; }
-                // the raw stage into registers and released at once, so that
-                // its next copy overlaps the wait for a free converted stage
-                constexpr int NCH = (BN * 4) / W8_GROUP_THREADS;   // 16-byte chunks a thread
-                uint4 v[NCH];
-                const uint8_t *raw = sQ + r * C::RAW_BYTES;
-#pragma unroll
-                for (int p = 0; p < NCH; ++p)
-                    v[p] = *reinterpret_cast<const uint4 *>(raw + (gt + p * W8_GROUP_THREADS) * 16);
-                mbar_arrive(&q_empty[r + loads_done(v)]);
-                if (!stage_free(ab_empty, seq, dev_error)) { ok = false; break; }
+                if (!mbar_wait(&q_full[r], rph, dev_error) ||
+                    !stage_free(ab_empty, seq, dev_error)) {
+                    ok = false;
+                    break;
+                }
                 // the stage's last reader was the tensor core (async proxy):
                 // order its reads before these generic writes
                 fence_proxy_async_smem();
-                uint8_t *b = sB + s * C::B_BYTES;
-#pragma unroll
-                for (int p = 0; p < NCH; ++p) {
-                    const int chunk = gt + p * W8_GROUP_THREADS;
-                    const int row = chunk >> 2, part = chunk & 3;
-                    uint4 lo, hi;
-                    widen16(v[p], lo, hi);
-                    uint8_t *brow = b + row * 128;
-                    const int sw = row & 7;
-                    *reinterpret_cast<uint4 *>(brow + (((2 * part) ^ sw) << 4)) = lo;
-                    *reinterpret_cast<uint4 *>(brow + (((2 * part + 1) ^ sw) << 4)) = hi;
-                }
+                widen_stage<BN>(sQ + r * C::RAW_BYTES, sB + s * C::B_BYTES, gt);
                 fence_proxy_async_smem();     // generic-proxy writes -> visible to the MMA
                 mbar_arrive(&b_full[s]);
+                mbar_arrive(&q_empty[r]);
             }
         }
     } else if (warp == 1) {

@@ -232,3 +232,40 @@ def test_w8_forced_tiles_on_ragged_shapes(tile):
                        env=env, capture_output=True, text=True, timeout=900,
                        cwd=os.path.dirname(here))
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
+
+
+@pytest.mark.parametrize("tile", ["w8d16", "w8d32", "w8d64", "dec64", "256"])
+def test_w8_forced_tiles_deterministic_at_prefill_size(tile):
+    """Each int8 tile kernel, forced, gives byte-identical FFN output (the
+    permuted rows y and the hidden rows h) over three runs of an OLMoE int8
+    T=2048 batch: the widened weight stages are rewritten while the next
+    stages are read, so a missing ordering shows up as run-to-run changes."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path.insert(0, %r); sys.path.insert(0, %r)\n"
+        "import torch\n"
+        "import __graft_entry__ as g; g.build()\n"
+        "from grouped_expert_gemm_moe_gb300 import binding as B, layer as L, workloads as W\n"
+        "import test_gpu_w8_stack as t\n"
+        "layer, inp, _ = t.w8_layer(B, L)\n"
+        "sh = W.OLMOE_W8\n"
+        "x, logits = t.batch(sh, 2048, 'uniform', inp.w_r, 3)\n"
+        "b = layer.buffers(2048)\n"
+        "layer.route(logits.to('cuda:0'), b); layer.permute(x.to('cuda:0'), b)\n"
+        "M = layer.rows(2048)\n"
+        "outs = []\n"
+        "for rep in range(3):\n"
+        "    b.ffn_ws.zero_(); b.y_perm.zero_()\n"
+        "    layer.ffn(b, 'gemm'); torch.cuda.synchronize(); layer.check()\n"
+        "    outs.append((b.ffn_ws[:M * sh.I * 2].clone(), b.y_perm[:M].clone()))\n"
+        "for h, y in outs[1:]:\n"
+        "    assert torch.equal(h, outs[0][0]) and torch.equal(y, outs[0][1]), 'runs differ'\n"
+        "print('deterministic')\n"
+    ) % (os.path.dirname(here), here)
+    env = dict(os.environ, MOE_GEMM_TILE=tile)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "deterministic" in r.stdout, r.stdout + r.stderr
