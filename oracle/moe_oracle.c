@@ -44,7 +44,7 @@
  * change any token's arithmetic.
  *
  * Return codes: 0 ok, 1 bad argument, 2 bad input value (expert id out of
- * range, NaN logit).
+ * range, non-finite logit).
  */
 #include <math.h>
 #include <stdint.h>
@@ -85,7 +85,7 @@ int oracle_route(const float *logits, int64_t T, int E, int k, int renormalize,
     for (int64_t t = 0; t < T && rc == OR_OK; ++t) {
         const float *L = logits + t * E;
         for (int e = 0; e < E; ++e)
-            if (isnan(L[e])) rc = OR_BAD_VALUE;
+            if (!isfinite(L[e])) rc = OR_BAD_VALUE;   /* NaN or +-inf: no softmax */
         if (rc != OR_OK) break;
         memset(taken, 0, (size_t)E);
         /* selection: k times, the best expert not yet taken */

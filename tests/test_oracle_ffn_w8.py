@@ -178,25 +178,56 @@ def test_quantize_exact_power_of_two_multiples():
     assert (s == np.float32(1 / 64)).all()
 
 
-def test_w8_layer_equals_bf16_layer_when_dequant_is_exact():
-    """Weights that int8 represents exactly: the w8 layer must equal the bf16
-    layer of the same weights."""
+def _exact_w8_matrix(rng, p, K):
+    """[..., N, K] matrix whose row n is m * 2^-p[..., n], max |m| = 127 on
+    every row, with m returned as well."""
+    m = rng.integers(-127, 128, size=p.shape + (K,))
+    col = rng.integers(0, K, size=p.shape)
+    np.put_along_axis(m, col[..., None], (127 * rng.choice([-1, 1], size=p.shape))[..., None],
+                      axis=-1)
+    return m * np.exp2(-p.astype(np.float64))[..., None], m
+
+
+def test_w8_layer_equals_bf16_layer_with_distinct_row_scales():
+    """Weights that int8 represents exactly, with a different power-of-two
+    scale on every row (gate row i, up row I+i and each down row n all
+    differ): the quantiser must return q = m and scale = 2^-p exactly, and
+    the w8 layer must equal the bf16 layer of the same weights.  Scales
+    applied to the wrong rows (gate/up swapped, down reversed, another
+    expert's) must break the equality, so the check can see such a slip."""
     rng = np.random.default_rng(13)
     T, H, I, E, S, k = 6, 32, 16, 4, 1, 2
-    def exact(shape):
-        m = rng.integers(-127, 128, size=shape)
-        m[..., 0] = 127
-        return m / 4096.0
-    wgu = bits(exact((E + S, 2 * I, H)))
-    wd = bits(exact((E + S, H, I)))
+    G = E + S
+    p_gate = rng.integers(6, 11, size=(G, I))
+    p_up = p_gate + rng.integers(1, 4, size=(G, I))          # up row I+i != gate row i
+    p_gu = np.concatenate([p_gate, p_up], axis=1)
+    p_down = rng.integers(6, 14, size=(G, H))
+    assert (p_down != p_down[:, ::-1]).any() and (p_down[:-1] != p_down[1:]).any()
+    wgu_v, m_gu = _exact_w8_matrix(rng, p_gu, H)
+    wd_v, m_d = _exact_w8_matrix(rng, p_down, I)
+    wgu, wd = bits(wgu_v), bits(wd_v)
     qg, sg = oracle.quantize_w8(wgu)
     qd, sd = oracle.quantize_w8(wd)
+    np.testing.assert_array_equal(qg, m_gu.astype(np.int8))
+    np.testing.assert_array_equal(qd, m_d.astype(np.int8))
+    np.testing.assert_array_equal(sg, np.exp2(-p_gu).astype(np.float32))
+    np.testing.assert_array_equal(sd, np.exp2(-p_down).astype(np.float32))
     x = rand_bf16(rng, (T, H), 1.0)
     L = rng.standard_normal((T, E)).astype(np.float32)
     ids, w = oracle.route(L, k, renormalize=True)
-    y8 = oracle.moe_layer_w8(x, ids, w, E, S, qg, sg, qd, sd)
     y16 = oracle.moe_layer(x, ids, w, E, S, wgu, wd)
+    y8 = oracle.moe_layer_w8(x, ids, w, E, S, qg, sg, qd, sd)
     np.testing.assert_allclose(y8, y16, rtol=1e-12, atol=1e-15)
+    # negative controls: the same comparison must fail for misapplied scales
+    wrong = {
+        "gate/up scales swapped": (np.concatenate([sg[:, I:], sg[:, :I]], 1), sd),
+        "down scales reversed": (sg, np.ascontiguousarray(sd[:, ::-1])),
+        "next expert's scales": (np.roll(sg, 1, axis=0), np.roll(sd, 1, axis=0)),
+    }
+    for what, (sg_x, sd_x) in wrong.items():
+        y_x = oracle.moe_layer_w8(x, ids, w, E, S, qg, sg_x, qd, sd_x)
+        rel = np.abs(y_x - y16).max() / np.abs(y16).max()
+        assert rel > 1e-3, f"{what}: not detected (max rel diff {rel:.2e})"
 
 
 def test_router_logits_vs_library_matmul():

@@ -112,9 +112,12 @@ def test_route_shift_invariance():
     np.testing.assert_allclose(w, w2, rtol=1e-12)
 
 
-def test_route_rejects_nan():
+@pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
+def test_route_rejects_non_finite_logits(bad):
+    """A NaN or infinite logit leaves the softmax without a finite value
+    (inf - inf), so such a row is refused rather than given NaN weights."""
     L = np.zeros((2, 4), np.float32)
-    L[1, 2] = np.nan
+    L[1, 2] = bad
     with pytest.raises(ValueError):
         oracle.route(L, 2, renormalize=False)
 
