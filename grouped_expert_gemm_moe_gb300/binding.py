@@ -60,6 +60,7 @@ _SIGS = {
     "moe_grouped_gemv_noalloc": ([P, P, I, I, I, I, P, P, P, P, P], I),
     "moe_route_permute": ([P, I, I, I, I, I, P, I, I, P, P, P, P, P, P, P, P], I),
     "moe_copy": ([P, P, SZ, P], I),
+    "moe_selftest_bounded_wait": ([I, I, ctypes.c_uint64, P, P, P], I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -444,3 +445,16 @@ def moe_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
         if not t.is_cuda and not t.is_pinned():
             raise ValueError("moe_copy: host tensors must be pinned")
     _ok(_lib.moe_copy(_ptr(dst), _ptr(src), dst.nbytes, _stream(stream)), "moe_copy")
+
+
+def moe_selftest_bounded_wait(kind: int, satisfiable: bool, limit_ns: int,
+                              counters: torch.Tensor, dev_error: torch.Tensor,
+                              stream=None) -> None:
+    """Run one bounded device wait (0: grid barrier, 1: mbarrier, 2: warp-
+    uniform mbarrier) on a condition met or never met; counters: 2 int32
+    words on the device."""
+    if counters.numel() < 2 or counters.dtype != torch.int32 or not counters.is_cuda:
+        raise ValueError("moe_selftest_bounded_wait: counters must be >= 2 int32 device words")
+    _ok(_lib.moe_selftest_bounded_wait(int(kind), int(bool(satisfiable)), int(limit_ns),
+                                       _ptr(counters), _ptr(dev_error), _stream(stream)),
+        "moe_selftest_bounded_wait")

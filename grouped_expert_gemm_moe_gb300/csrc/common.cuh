@@ -180,13 +180,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Wait until the phase of `bar` with the given parity has completed.  The
 // wait is bounded: on running out it reports MOE_ERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *dev_error) {
+// (The limit is an argument only so that moe_selftest_bounded_wait can run
+// this very code with a short one; kernels use the default.)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *dev_error,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t polls = 1;; ++polls) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((polls & 255u) == 0 &&
-            (globaltimer() - t0 > WAIT_LIMIT_NS || polls >= WAIT_LIMIT_POLLS)) {
+            (globaltimer() - t0 > limit_ns || polls >= WAIT_LIMIT_POLLS)) {
             report(dev_error, MOE_ERR_TIMEOUT);
             return false;
         }
@@ -197,8 +200,44 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
 // the warp-collective tcgen05.ld / tcgen05.st after it need every lane, even
 // when the time limit runs out in some lanes only.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
-                                               int32_t *dev_error) {
-    return __all_sync(FULL, mbar_wait(bar, parity, dev_error));
+                                               int32_t *dev_error,
+                                               uint64_t limit_ns = WAIT_LIMIT_NS) {
+    return __all_sync(FULL, mbar_wait(bar, parity, dev_error, limit_ns));
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier of a launch whose CTAs are all resident (a cooperative
+// launch): every CTA adds one to *count and waits until it reaches `target`
+// (the caller zeroes the word before the launch and raises the target by
+// gridDim.x per barrier).  Writes before the barrier are visible to every CTA
+// after it.  The wait is bounded: on running out thread 0 reports
+// MOE_ERR_TIMEOUT and sets *fail (a shared word the CTA initialised to 0),
+// and every thread of the CTA gets false.
+__device__ __forceinline__ bool grid_barrier(unsigned *count, unsigned target, int *fail,
+                                             int32_t *dev_error,
+                                             uint64_t limit_ns = WAIT_LIMIT_NS) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(count, 1u);
+        const uint64_t t0 = globaltimer();
+        for (uint32_t polls = 0;; ++polls) {
+            if (ld_acquire_gpu(count) >= target) break;
+            if ((polls & 63u) == 63u && globaltimer() - t0 > limit_ns) {
+                report(dev_error, MOE_ERR_TIMEOUT);
+                *reinterpret_cast<volatile int *>(fail) = 1;
+                break;
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return *reinterpret_cast<volatile int *>(fail) == 0;
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {

@@ -45,35 +45,6 @@ struct DecodePlan {
     int fail;
 };
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// All CTAs of the grid arrive; returns when `target` arrivals are counted
-// (bounded).  Writes before the barrier are visible to every CTA after it.
-__device__ __forceinline__ bool grid_barrier(unsigned *count, unsigned target, DecodePlan &pl,
-                                             int32_t *dev_error) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(count, 1u);
-        const uint64_t t0 = globaltimer();
-        for (uint32_t polls = 0;; ++polls) {
-            if (ld_acquire_gpu(count) >= target) break;
-            if ((polls & 63u) == 63u && globaltimer() - t0 > WAIT_LIMIT_NS) {
-                report(dev_error, MOE_ERR_TIMEOUT);
-                pl.fail = 1;
-                break;
-            }
-        }
-        __threadfence();
-    }
-    __syncthreads();
-    return !pl.fail;
-}
-
 template <int PER_LANE>
 __global__ void __launch_bounds__(DL_THREADS, 2) decode_layer_kernel(
     const float *__restrict__ logits, const uint16_t *__restrict__ x, int T, int E, int S, int k,
@@ -176,7 +147,7 @@ __global__ void __launch_bounds__(DL_THREADS, 2) decode_layer_kernel(
             }
         }
     }
-    if (!grid_barrier(barrier, gridDim.x, pl, dev_error)) return;
+    if (!grid_barrier(barrier, gridDim.x, &pl.fail, dev_error)) return;
 
     // ---------------------------------------------------------- phase 2
     {
@@ -204,7 +175,7 @@ __global__ void __launch_bounds__(DL_THREADS, 2) decode_layer_kernel(
             }
         }
     }
-    if (!grid_barrier(barrier, 2u * gridDim.x, pl, dev_error)) return;
+    if (!grid_barrier(barrier, 2u * gridDim.x, &pl.fail, dev_error)) return;
     pdl_trigger();
 
     // ---------------------------------------------------------- phase 3

@@ -1,8 +1,9 @@
 // gemm_tc.cu -- all-experts grouped GEMM on the 5th-generation tensor cores.
 //
-// "A tensor-core grouped GEMM with SwiGLU fused into its epilogue", all
-// experts in one launch ("switchyard" page, 02 Kernels and dispatch, "One
-// launch for all experts").  Written for sm_103a:
+// One launch covers every expert, with the SwiGLU activation applied in the
+// GEMM's epilogue, as the "switchyard" page (02 Kernels and dispatch, "One
+// launch for all experts") describes for its tensor-core kernel.  Written
+// for sm_103a:
 //
 //  * persistent grid, one CTA per SM; a per-expert tile scheduler walks the
 //    linear tile index over (group g, n-tile, m-tile) with the m-tile

@@ -1,7 +1,8 @@
 // gemv.cu -- grouped GEMV for decode-sized batches (bf16 and int8 weights).
 //
-// "For decode, a grouped GEMV at 73% of memory bandwidth" ("switchyard"
-// page, 02 Kernels and dispatch, "One launch for all experts").  With a few
+// The "switchyard" page (02 Kernels and dispatch, "One launch for all
+// experts") serves decode with a grouped GEMV that it measured at 73 % of
+// the T4's memory bandwidth.  With a few
 // rows per expert the FFN is a weight stream: every expert weight row is
 // read from HBM once, with coalesced 128-bit loads (a warp reads 512
 // contiguous bytes per instruction), and dotted with the handful of
@@ -552,19 +553,14 @@ extern "C" moe_status moe_grouped_gemv_noalloc(const uint16_t *x_perm, const int
                                                int G, int M, int H, int I, const uint16_t *w_gu,
                                                const uint16_t *w_down, uint16_t *y_perm,
                                                int32_t *dev_error, cudaStream_t stream) {
-    if (!x_perm || !offsets || !w_gu || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
-    if (G < 1 || M < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
-    if (G > 1024) return MOE_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(M) * H >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
-    if (H % 8 != 0 || I % 8 != 0) return MOE_ERR_ALIGNMENT;
-    if (!aligned16(x_perm) || !aligned16(w_gu) || !aligned16(w_down) || !aligned16(y_perm))
-        return MOE_ERR_ALIGNMENT;
-    // the built-in scratch holds h = M x I bf16; a larger problem is refused
-    if (static_cast<size_t>(M) * static_cast<size_t>(I) * 2 > NOALLOC_SCRATCH_BYTES)
-        return MOE_ERR_WORKSPACE;
     moe_status st = MOE_OK;
     uint16_t *h = noalloc_scratch(&st);
     if (h == nullptr) return st;
+    // The same argument checks as moe_grouped_gemv, with the built-in array
+    // as the workspace: h = M x I bf16 must fit in it, else MOE_ERR_WORKSPACE.
+    st = check_ffn_args(x_perm, offsets, G, M, H, I, w_gu, w_down, y_perm, h,
+                        NOALLOC_SCRATCH_BYTES, 8);
+    if (st != MOE_OK) return st;
     // Nothing in the scratch has to start at zero: the gate/up pass writes
     // every h row of every non-empty group before the down pass reads it.
     launch_gateup_bf16(pick_nch(H / 8), pick_nr(M, G), stream, x_perm, offsets, G, M, H, I, w_gu, h, dev_error);

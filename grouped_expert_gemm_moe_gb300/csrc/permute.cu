@@ -1,7 +1,8 @@
 // permute.cu -- stable sort of token slots by expert, and the row gather.
 //
-// "Rows sorted by expert with a block-wide prefix scan and no atomics"
-// ("switchyard" page, 02 Kernels and dispatch, "Route and sort").
+// The "switchyard" page (02 Kernels and dispatch, "Route and sort") orders
+// the token rows by expert using a prefix scan over the whole block, with
+// no atomic operations; this file does the same on sm_103a.
 //
 // The building block is a block-wide ranking of up to 1024 slots (one per
 // thread, in slot order): each warp groups its 32 slots by expert with a

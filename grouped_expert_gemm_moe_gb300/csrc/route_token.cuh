@@ -18,7 +18,8 @@ namespace moe {
 
 // Routes one token with the calling warp.  Lane j < k receives the j-th
 // chosen expert and its weight.  Returns false (on every lane) if a logit is
-// NaN, leaving the outputs undefined.
+// not finite (NaN or +-inf: the softmax of such a row has no finite
+// weights), leaving the outputs undefined.
 template <int PER_LANE>
 __device__ __forceinline__ bool route_token(const float *L, int E, int k,
                                             int renormalize, int &my_id, float &my_w) {
@@ -29,7 +30,7 @@ __device__ __forceinline__ bool route_token(const float *L, int E, int k,
     for (int i = 0; i < PER_LANE; ++i) {
         const int e = lane + 32 * i;
         v[i] = e < E ? L[e] : -INFINITY;          // global or shared memory
-        nan_seen |= isnan(v[i]);
+        nan_seen |= e < E && !isfinite(v[i]);
     }
     if (__any_sync(FULL, nan_seen)) return false;
 

@@ -34,7 +34,7 @@
  *    elements.  Otherwise MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED.
  *  - The return value reports what the host can see: argument checks and
  *    launch errors (cudaGetLastError -> MOE_ERR_CUDA).  Faults in the data
- *    (an expert id outside [0,E), a NaN logit, inconsistent offsets) are
+ *    (an expert id outside [0,E), a non-finite logit, inconsistent offsets) are
  *    found on the device: the kernel skips the offending write and stores
  *    MOE_ERR_DEVICE_CHECK into *dev_error; a bounded wait that ran out
  *    stores MOE_ERR_TIMEOUT.  dev_error is one int32 in device memory that
@@ -111,7 +111,8 @@ moe_status moe_router_route(const uint16_t *x, const uint16_t *w_r, const float 
  * largest logit in descending order, ties broken toward the lower expert
  * index.  topk_w: [T,k] fp32, softmax over all E logits of each chosen
  * expert; if `renormalize` is non-zero the k weights are divided by their
- * sum.  A NaN logit is a device-check fault (that token's outputs are
+ * sum.  A non-finite logit (NaN or +-inf, for which the softmax has no
+ * finite value) is a device-check fault (that token's outputs are
  * left untouched).  E <= 1024.
  */
 moe_status moe_route(const float *logits, int T, int E, int k, int renormalize,
@@ -178,7 +179,7 @@ moe_status moe_permute_capped(const int32_t *topk_ids, int T, int E, int S, int 
  * decode-sized batches (T*k <= 1024 slots, E <= 256; otherwise
  * MOE_ERR_UNSUPPORTED and nothing is launched).  Same arguments and the same
  * outputs, bit for bit, as the two calls (no permute workspace is needed);
- * a NaN logit is a device-check fault that leaves every group empty.  The
+ * a non-finite logit is a device-check fault that leaves every group empty.  The
  * pages route and sort in separate steps ("switchyard" page, "Route and
  * sort"); fusing them removes a launch and a round trip through global
  * memory from the latency-bound decode step.
@@ -377,6 +378,29 @@ moe_status moe_copy(void *dst, const void *src, size_t bytes, cudaStream_t strea
  */
 moe_status moe_quantize_w8(const uint16_t *w_host, int64_t rows, int64_t K, int8_t *q_host,
                            float *scale_host);
+
+/*
+ * moe_selftest_bounded_wait -- runs one of the library's bounded device
+ * waits, with a short limit, on a condition that is met (satisfiable != 0)
+ * or never met, so that a test can see the failure-detection path work
+ * without faulting or hanging the GPU.  The pages have no counterpart: it
+ * exercises this library's own rule that no device wait is unbounded.
+ *   kind 0: the grid barrier of moe_decode_layer (a cooperative launch of 2
+ *           CTAs; the unmet form waits for one arrival more than the grid
+ *           makes);
+ *   kind 1: one thread's mbarrier wait of the tensor-core kernels (the unmet
+ *           form waits on an mbarrier nobody arrives at);
+ *   kind 2: the warp-uniform mbarrier wait that precedes tcgen05.ld / .st.
+ * limit_ns: the wait's limit in ns of %globaltimer, 1e3 .. 1e10 (the
+ * kernels themselves use 1 s).  counters: 2 device words, zeroed by the
+ * call; counters[0] = grid-barrier arrivals (kind 0: ends at 2),
+ * counters[1] = waits that completed (kind 0: 2 CTAs, kind 1: 1, kind 2: 32
+ * lanes; 0 when the limit ran out).  When a limit runs out the kernel
+ * writes MOE_ERR_TIMEOUT to *dev_error and returns; nothing else is in
+ * flight.  Asynchronous on `stream`.
+ */
+moe_status moe_selftest_bounded_wait(int kind, int satisfiable, uint64_t limit_ns,
+                                     unsigned *counters, int32_t *dev_error, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

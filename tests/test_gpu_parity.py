@@ -241,12 +241,13 @@ def test_invalid_expert_id_is_reported_without_out_of_bounds(B, L, T):
     assert int(layer.err.item()) == 6       # combine skipped the unplaced slots
 
 
-def test_nan_logit_is_reported(B, L):
+@pytest.mark.parametrize("bad", [float("nan"), float("inf"), float("-inf")])
+def test_non_finite_logit_is_reported(B, L, bad):
     inp, _ = layer_case("tiny", 16, "uniform")
     layer = make_layer_obj(L, inp)
     b = layer.buffers(16)
     logits = inp.logits.clone()
-    logits[2, 3] = float("nan")
+    logits[2, 3] = bad
     layer.route(logits.to(DEV), b)
     torch.cuda.synchronize()
     assert int(layer.err.item()) == 6
