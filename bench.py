@@ -96,8 +96,10 @@ def load_peaks():
 # headers they include): a committed traffic figure is used only while these
 # are unchanged since the counters were taken.
 KERNEL_SOURCES = {
-    "tc_grouped_gemm_swiglu": ("gemm_tc.cu", "gemm_tc_pair.cu", "gemm_tc_dec.cu",
-                               "gemm_tc256.cu", "tc_common.cuh", "tc_pair.cuh", "common.cuh"),
+    "tc_grouped_gemm_swiglu": ("gemm_tc.cu", "gemm_tc_pair.cu", "tc_common.cuh", "tc_pair.cuh",
+                               "common.cuh"),
+    "tc_grouped_gemm_dec_w8": ("gemm_tc_dec_w8.cu", "gemm_tc_w8.cu", "gemm_tc.cu", "tc_w8.cuh",
+                               "tc_common.cuh", "common.cuh"),
     "decode_layer_kernel": ("decode_layer.cu", "gemv_tasks.cuh", "route_token.cuh",
                             "common.cuh"),
     "gemv_gateup_bf16": ("gemv.cu", "gemv_tasks.cuh", "common.cuh"),
@@ -193,6 +195,69 @@ class ClockSampler:
                 "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
+class NvmlSampler:
+    """SM clock, max SM clock and clock-event reasons every ~1 ms from a
+    host thread through NVML's C API (the driver's libnvidia-ml.so.1, loaded
+    with ctypes), so that a timed region of a few milliseconds still holds
+    samples; stop(t0, t1) keeps the samples inside the wall-clock window.
+    `ok` is False when NVML cannot be used (ClockSampler is used then)."""
+
+    # nvmlClocksEventReasons bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, gpu_index: int, period_s: float = 0.001):
+        import ctypes
+        import threading
+        self.ok = False
+        self.samples = []
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(h)) != 0:
+                return
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            return
+        self.nv, self.h, self.reasons_fn = nv, h, reasons_fn
+        mx = ctypes.c_uint(0)
+        self.max_mhz = (float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+                        == 0 else None)
+        self.period = period_s
+        self.stop_flag = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.ok = True
+        self.thread.start()
+
+    def _run(self):
+        import ctypes
+        mhz = ctypes.c_uint(0)
+        rs = ctypes.c_ulonglong(0)
+        while not self.stop_flag.is_set():
+            t = time.time()
+            a = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz))   # NVML_CLOCK_SM
+            b = self.reasons_fn(self.h, ctypes.byref(rs))
+            if a == 0 and b == 0:
+                self.samples.append((t, float(mhz.value), int(rs.value)))
+            time.sleep(self.period)
+
+    def stop(self, t0: float, t1: float):
+        if not self.ok:
+            return None
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        use = inside if inside else self.samples
+        sm = [x[1] for x in use]
+        reasons = sorted({name for x in use for name, bit in self.BITS.items() if x[2] & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "source": "NVML, ~1 ms period"}
+
+
 # ------------------------------------------------------------ workload
 
 def build_workload(name, device, seed):
@@ -217,8 +282,9 @@ def extra_batch(shape, T, routing, seed, device, inp):
 
 class Phases:
     """One layer step recorded as three CUDA graphs -- [route, permute],
-    [gate/up], [down, combine] -- so the dominant kernel can be timed with
-    events between graph launches inside the timed region."""
+    [gate/up] (bf16 experts; the whole FFN for int8 experts, whose two GEMMs
+    are one call), [down, combine] -- so the dominant kernel can be timed
+    with events between graph launches inside the timed region."""
 
     def __init__(self, layer, x, logits, kind):
         import torch
@@ -229,10 +295,14 @@ class Phases:
             layer.route_permute(logits, x, b)
 
         def mid():
-            layer.gate_up(b, kind)
+            if layer.int8:
+                layer.ffn(b, kind)
+            else:
+                layer.gate_up(b, kind)
 
         def post():
-            layer.down(b, kind)
+            if not layer.int8:
+                layer.down(b, kind)
             layer.combine(b, b.out)
 
         self.graphs = []
@@ -318,12 +388,19 @@ def time_steps(phases, K, W, flush):
     return step, gate_up
 
 
-def layer_roofline(shape, T, n_groups, peaks):
-    """Ideal layer time: max(FLOPs / bf16 peak, algorithmic bytes / HBM BW).
-    Bytes: weights of served groups (3*H*I*2) + x in + out (T*H*2 each);
-    FLOPs: 6*H*I per served row (routed slots + shared rows)."""
+def weight_bytes_per_group(shape, int8: bool) -> int:
+    """Algorithmic weight bytes of one served group: bf16 3*H*I*2; int8
+    3*H*I plus the fp32 scales of its 2I + H output rows."""
     H, I = shape.H, shape.I
-    bytes_ = n_groups * 3 * H * I * 2 + 2 * T * H * 2
+    return 3 * H * I + (2 * I + H) * 4 if int8 else 3 * H * I * 2
+
+
+def layer_roofline(shape, T, n_groups, peaks, int8=False):
+    """Ideal layer time: max(FLOPs / bf16 peak, algorithmic bytes / HBM BW).
+    Bytes: weights of served groups + x in + out (T*H*2 each); FLOPs:
+    6*H*I per served row (routed slots + shared rows)."""
+    H, I = shape.H, shape.I
+    bytes_ = n_groups * weight_bytes_per_group(shape, int8) + 2 * T * H * 2
     flops = 6.0 * H * I * shape.rows(T)
     t_mem = bytes_ / (peaks["hbm_gbs"] * 1e9)
     t_flop = flops / (peaks["bf16_tflops"] * 1e12)
@@ -331,38 +408,49 @@ def layer_roofline(shape, T, n_groups, peaks):
                 bound="hbm" if t_mem >= t_flop else "tensor")
 
 
-def kernel_roofline(shape, T, n_groups, gate_up_ms, peaks, kind, workload):
-    """Roofline of the gate/up kernel: its algorithmic bytes are the gate and
-    up weights of the served groups (2*I*H*2 per group); its FLOPs are
-    4*H*I per served row."""
+def kernel_roofline(shape, T, n_groups, gate_up_ms, peaks, kind, workload, int8=False):
+    """Roofline of the dominant kernel.  bf16: the gate/up GEMM, whose
+    algorithmic bytes are the gate and up weights of the served groups
+    (2*I*H*2 per group) and whose FLOPs are 4*H*I per served row.  int8:
+    the whole FFN (both GEMMs are one call), bytes as weight_bytes_per_group,
+    FLOPs 6*H*I per served row.  Both fractions are given; `bound` names the
+    one the roofline says limits it."""
     H, I = shape.H, shape.I
-    bytes_ = n_groups * 2 * I * H * 2
-    flops = 4.0 * H * I * shape.rows(T)
+    if int8:
+        bytes_ = n_groups * weight_bytes_per_group(shape, True)
+        flops = 6.0 * H * I * shape.rows(T)
+        name = "tc_grouped_gemm_dec_w8" if kind == "gemm" else "gemv_gateup_w8"
+    else:
+        bytes_ = n_groups * 2 * I * H * 2
+        flops = 4.0 * H * I * shape.rows(T)
+        name = "tc_grouped_gemm_swiglu" if kind == "gemm" else "gemv_gateup_bf16"
     sec = gate_up_ms / 1e3
     t_mem = bytes_ / (peaks["hbm_gbs"] * 1e9)
     t_flop = flops / (peaks["bf16_tflops"] * 1e12)
-    name = "tc_grouped_gemm_swiglu" if kind == "gemm" else "gemv_gateup_bf16"
     traffic = profiled_traffic(name, workload)
+    gbs = bytes_ / sec / 1e9
+    tfs = flops / sec / 1e12
+    both = {"hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "tensor_frac": round(tfs / peaks["bf16_tflops"], 4),
+            "hbm_frac_of_nominal_8tbs": round(gbs / 8000.0, 4)}
     if t_mem >= t_flop:
-        ach = bytes_ / sec / 1e9
-        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": traffic, "algorithmic_bytes": bytes_,
+        return {"kernel": name, "bound": "hbm", "achieved": round(gbs, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": both["hbm_frac"],
+                "traffic": traffic, "algorithmic_bytes": bytes_, **both,
                 "avg_launch_us": round(gate_up_ms * 1e3, 2),
                 "peak_source": f"{peaks['source']} (STREAM copy, burst)"}
-    ach = flops / sec / 1e12
-    return {"kernel": name, "bound": "tensor", "achieved": round(ach, 1),
-            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
-            "algorithmic_flops": flops, "avg_launch_us": round(gate_up_ms * 1e3, 2),
+    return {"kernel": name, "bound": "tensor", "achieved": round(tfs, 1),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": both["tensor_frac"],
+            "traffic": traffic, "algorithmic_flops": flops, "algorithmic_bytes": bytes_,
+            **both, "avg_launch_us": round(gate_up_ms * 1e3, 2),
             "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
 
 
 def measure_T(layer, shape, T, x, logits, K, W, flush, peaks, workload, ffn="auto"):
     """Layer time from K steps of the whole forward pass captured in one
-    CUDA graph; the gate/up kernel's time from K further steps recorded as
-    three graphs with events around the gate/up launch.  ffn: "auto" (the
-    layer's own choice) or a forced "decode", "gemv" or "gemm"."""
+    CUDA graph; the dominant kernel's time from K further steps recorded as
+    three graphs with events around it.  ffn: "auto" (the layer's own
+    choice) or a forced "decode", "gemv" or "gemm"."""
     kind = layer.choose_path(T, x.dtype) if ffn == "auto" else ffn
     if kind == "decode" and not layer.decode_layer_ok(T, x.dtype):
         raise SystemExit(f"--ffn decode: T={T} is outside the fused decode layer's limits")
@@ -381,11 +469,11 @@ def measure_T(layer, shape, T, x, logits, K, W, flush, peaks, workload, ffn="aut
     ph = Phases(layer, x, logits, kind)
     _, gu = time_steps(ph, K, W, flush)
     n_groups = touched_groups(layer, ph.b)
-    roof = layer_roofline(shape, T, n_groups, peaks)
+    roof = layer_roofline(shape, T, n_groups, peaks, layer.int8)
     return dict(kind=kind, step_ms=step, gate_up_ms=statistics.fmean(gu), ms=ms,
                 n_groups=n_groups, roof=roof,
                 kroof=kernel_roofline(shape, T, n_groups, statistics.fmean(gu), peaks, kind,
-                                      workload))
+                                      workload, layer.int8))
 
 
 def decode_kernel_roofline(shape, T, n_groups, step_ms, peaks, workload):
@@ -397,6 +485,8 @@ def decode_kernel_roofline(shape, T, n_groups, step_ms, peaks, workload):
     ach = bytes_ / (step_ms / 1e3) / 1e9
     return {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": round(ach, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+            "hbm_frac": round(ach / peaks["hbm_gbs"], 4),
+            "hbm_frac_of_nominal_8tbs": round(ach / 8000.0, 4),
             "traffic": profiled_traffic("decode_layer_kernel", workload),
             "algorithmic_bytes": bytes_, "avg_launch_us": round(step_ms * 1e3, 2),
             "peak_source": f"{peaks['source']} (STREAM copy, burst)"}
@@ -429,46 +519,102 @@ def e2e_measure(layer, shape, T, inp, K, W, flush, ffn="auto"):
     return ms, h2d, d2h, cap.out_host.clone()
 
 
-def other_rows(dev, K, W, flush, peaks):
-    """The int8 weight-only layer (OLMoE shapes, T=64, uniform routing), the
-    capacity-limited (token-dropping) layer at the pages' 4x load skew
-    (T=2048, dropless / CF 2.0 / CF 1.0) and the 16-layer OLMoE-shaped stack
-    (skewed routing, T=64 and T=2048), each
-    captured in one CUDA graph and timed like the main workload: W warm-up
-    steps, then K (capped for the long stack steps) timed steps with L2
-    flushed before each.  Rooflines: weight bytes of the served groups at
-    HBM bandwidth vs FLOPs at the bf16 peak (sustained for the stack, whose
-    steps run for milliseconds), per layer, summed over the stack."""
-    import numpy as np
+# The sweep of other_rows: (row prefix, shape config, routing, token counts,
+# int8 experts).  The token counts are the configs' own: OLMoE decode 1/8/64
+# (and the 2048-token prefill), DeepSeek 1..2048 under uniform and zipf
+# routing, OLMoE int8 at 7 token counts under both routings, and the DeepSeek
+# shapes in int8 as the secondary sweep.
+SWEEP = (
+    ("olmoe", "olmoe", "uniform", (1, 8, 64, 2048), False),
+    ("deepseek", "deepseek", "uniform", (1, 16, 128, 512, 2048), False),
+    ("deepseek_zipf", "deepseek", "zipf", (1, 16, 128, 512, 2048), False),
+    ("olmoe_int8", "olmoe", "uniform", (1, 8, 16, 64, 128, 512, 2048), True),
+    ("olmoe_int8_zipf", "olmoe", "zipf", (1, 8, 16, 64, 128, 512, 2048), True),
+    ("deepseek_int8", "deepseek", "uniform", (1, 16, 128, 512, 2048), True),
+    ("deepseek_int8_zipf", "deepseek", "zipf", (1, 16, 128, 512, 2048), True),
+)
+
+
+def row_of(m, T):
+    """One table row from measure_T's result."""
+    kr = m["kroof"]
+    row = {"us_per_layer": round(m["ms"] * 1e3, 2),
+           "tokens_per_s": round(T / (m["ms"] / 1e3), 1), "ffn": m["kind"],
+           "groups": m["n_groups"], "layer_bound": m["roof"]["bound"],
+           "layer_t_roof_us": round(m["roof"]["t_roof_us"], 2),
+           "layer_roofline_frac": round(m["roof"]["t_roof_us"] / (m["ms"] * 1e3), 4)}
+    label = ("layer" if m["kind"] == "decode" else
+             "ffn" if kr["kernel"].endswith("_w8") else "gate_up")
+    row[f"{label}_us"] = kr["avg_launch_us"]
+    row[f"{label}_hbm_frac"] = kr.get("hbm_frac", kr["frac"])
+    row[f"{label}_hbm_frac_of_nominal_8tbs"] = kr.get("hbm_frac_of_nominal_8tbs")
+    if "tensor_frac" in kr:
+        row[f"{label}_tensor_frac"] = kr["tensor_frac"]
+    return row
+
+
+def sweep_rows(dev, K, W, flush, peaks):
+    """Every (layer, routing, T) of SWEEP: the layer built once per shape and
+    weight type (seed 0), a fresh seeded batch per T, each T timed like the
+    headline (whole layer in one graph; the dominant kernel by events around
+    its own graph).  Steps capped at 100 per row."""
     import torch
 
     from grouped_expert_gemm_moe_gb300 import binding as B
     from grouped_expert_gemm_moe_gb300 import workloads as WL
+    from grouped_expert_gemm_moe_gb300.layer import MoELayer
+    rows = {}
+    K2 = max(3, min(K, 100))
+    built = {}
+    for prefix, cfg, routing, Ts, int8 in SWEEP:
+        key = (cfg, int8)
+        if key not in built:
+            built.clear()
+            torch.cuda.empty_cache()
+            sh = WL.CONFIGS[cfg]
+            inp = WL.make_layer(sh, 1, "uniform", seed=0, device=dev)
+            if int8:
+                q_gu, s_gu = B.moe_quantize_w8(inp.w_gu)
+                q_down, s_down = B.moe_quantize_w8(inp.w_down)
+                layer = MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize,
+                                 q_gu=q_gu.to(dev), s_gu=s_gu.to(dev), q_down=q_down.to(dev),
+                                 s_down=s_down.to(dev), device=dev)
+                inp.w_gu = inp.w_down = None
+            else:
+                layer = MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize, w_gu=inp.w_gu,
+                                 w_down=inp.w_down, device=dev)
+            built[key] = (sh, inp, layer)
+        sh, inp, layer = built[key]
+        bias = WL.routing_bias(sh, routing)
+        for T in Ts:
+            g = WL.make_generator(1000 + T, dev)
+            x = torch.randn((T, sh.H), generator=g, device=dev).to(torch.bfloat16)
+            logits = WL.router_logits_input(x, inp.w_r, None if bias is None else bias.to(dev))
+            m = measure_T(layer, sh, T, x, logits, K2, W, flush, peaks, f"{prefix}_t{T}")
+            layer.check()
+            rows[f"{prefix}_t{T}"] = {**row_of(m, T), "steps": K2}
+        layer._bufs.clear()
+    built.clear()
+    torch.cuda.empty_cache()
+    return rows
+
+
+def other_rows(dev, K, W, flush, peaks):
+    """The capacity-limited (token-dropping) layer at the pages' 4x load
+    skew (T=2048, dropless / CF 2.0 / CF 1.0) and the 16-layer OLMoE-shaped
+    stack (skewed routing, T=64 and T=2048), each captured in one CUDA graph
+    and timed like the main workload: W warm-up steps, then K (capped for the
+    long stack steps) timed steps with L2 flushed before each.  Rooflines:
+    weight bytes of the served groups at HBM bandwidth vs FLOPs at the bf16
+    peak (sustained for the stack, whose steps run for milliseconds), per
+    layer, summed over the stack."""
+    import numpy as np
+    import torch
+
+    from grouped_expert_gemm_moe_gb300 import workloads as WL
     from grouped_expert_gemm_moe_gb300.layer import MoELayer, MoEStack
     rows = {}
     bw = peaks["hbm_gbs"] * 1e9
-
-    sh = WL.OLMOE_W8
-    T = 64
-    inp = WL.make_layer(sh, T, "uniform", seed=0, device=dev)
-    q_gu, s_gu = B.moe_quantize_w8(inp.w_gu)
-    q_down, s_down = B.moe_quantize_w8(inp.w_down)
-    layer = MoELayer(sh.H, sh.E, sh.k, sh.I, 0, False, q_gu=q_gu.to(dev), s_gu=s_gu.to(dev),
-                     q_down=q_down.to(dev), s_down=s_down.to(dev), device=dev)
-    kind = layer.choose_ffn(T)
-    cap = layer.capture(inp.x, inp.logits, ffn=kind)
-    ms = statistics.fmean(time_graph(cap, K, W, flush))
-    layer.check()
-    ng = touched_groups(layer, layer.buffers(T))
-    H, I = sh.H, sh.I
-    bytes_ = ng * (3 * H * I + (2 * I + H) * 4) + 2 * T * H * 2
-    t_roof = max(bytes_ / bw, 6.0 * H * I * T * sh.k / (peaks["bf16_tflops"] * 1e12)) * 1e6
-    rows["int8_weight_only_t64"] = {
-        "us_per_layer": round(ms * 1e3, 2), "tokens_per_s": round(T / (ms / 1e3), 1),
-        "ffn": kind, "groups": ng, "algorithmic_bytes": bytes_, "bound": "hbm",
-        "t_roof_us": round(t_roof, 2), "roofline_frac": round(t_roof / (ms * 1e3), 4)}
-    del layer, cap, inp, q_gu, q_down
-    torch.cuda.empty_cache()
 
     # token dropping at the pages' load skew (busiest expert ~4x the mean),
     # OLMoE layer, T=2048: dropless vs capacity factors 2.0 and 1.0
@@ -644,9 +790,12 @@ def run_ours(args):
                               "parity": base["parity"]}))
             sys.exit(1)
 
-    sampler = ClockSampler(local) if rank == 0 else None
-    if sampler is not None:
-        time.sleep(0.5)                         # let nvidia-smi start sampling
+    sampler = None
+    if rank == 0:
+        sampler = NvmlSampler(local)
+        if not sampler.ok:
+            sampler = ClockSampler(local)
+            time.sleep(0.5)                     # let nvidia-smi start sampling
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -673,8 +822,9 @@ def run_ours(args):
                           "gate_up_frac": m2["kroof"]["frac"], "groups": m2["n_groups"]}
     layer.check()
 
-    rows = None
+    rows = sweep = None
     if world == 1 and not args.no_rows:
+        sweep = sweep_rows(dev, args.steps, args.warmup, flush, peaks)
         rows = other_rows(dev, args.steps, args.warmup, flush, peaks)
 
     e2e_ms, h2d, d2h, out_e2e = e2e_measure(layer, shape, T, inp, args.steps, args.warmup, flush,
@@ -709,6 +859,7 @@ def run_ours(args):
                                "peak_source": peaks["source"]},
             "roofline": m["kroof"],
             "per_T": per_T,
+            "sweep": sweep,
             "other_rows": rows,
             "e2e": {"value": round(aggregate_value(T * args.steps, world, e2e_sec), 1),
                     "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -785,7 +936,8 @@ def main(argv=None):
                     help="FFN path of the workload's layer: the layer's own choice, or "
                          "forced (to time or profile one path)")
     ap.add_argument("--no-rows", action="store_true",
-                    help="skip the int8 and 16-layer stack measurements of other_rows")
+                    help="skip the sweep over every config and the capacity and 16-layer "
+                         "stack measurements of other_rows")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -61,6 +61,7 @@ _SIGS = {
     "moe_route_permute": ([P, I, I, I, I, I, P, I, I, P, P, P, P, P, P, P, P], I),
     "moe_copy": ([P, P, SZ, P], I),
     "moe_selftest_bounded_wait": ([I, I, ctypes.c_uint64, P, P, P], I),
+    "moe_set_gemm_tile": ([I], I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -458,3 +459,31 @@ def moe_selftest_bounded_wait(kind: int, satisfiable: bool, limit_ns: int,
     _ok(_lib.moe_selftest_bounded_wait(int(kind), int(bool(satisfiable)), int(limit_ns),
                                        _ptr(counters), _ptr(dev_error), _stream(stream)),
         "moe_selftest_bounded_wait")
+
+
+# moe_tile values of include/moe.h
+GEMM_TILES = {"auto": -1, "128x128": 0, "128x256": 1, "pair": 2, "w8_d16": 3, "w8_d32": 4,
+              "w8_d64": 5, "w8_rows": 6}
+
+
+def moe_set_gemm_tile(tile: str = "auto") -> None:
+    """Force one tile kernel for every later grouped GEMM call ("auto":
+    the per-call choice by rows per group)."""
+    if tile not in GEMM_TILES:
+        raise ValueError(f"unknown tile {tile!r}; one of {sorted(GEMM_TILES)}")
+    _ok(_lib.moe_set_gemm_tile(GEMM_TILES[tile]), "moe_set_gemm_tile")
+
+
+class forced_gemm_tile:
+    """Context manager: the grouped GEMM calls inside use `tile`."""
+
+    def __init__(self, tile: str):
+        self.tile = tile
+
+    def __enter__(self):
+        moe_set_gemm_tile(self.tile)
+        return self
+
+    def __exit__(self, *exc):
+        moe_set_gemm_tile("auto")
+        return False

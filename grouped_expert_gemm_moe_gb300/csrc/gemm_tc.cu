@@ -32,6 +32,8 @@
 
 #include <algorithm>
 
+#include <atomic>
+
 #include "tc_common.cuh"
 
 namespace moe {
@@ -299,103 +301,76 @@ static moe_status launch_tc(const void *act, const void *w, const int32_t *offse
 using namespace moe;
 
 namespace moe {
-template <bool SWIGLU>
-moe_status launch_tc256(const void *act, const void *w, const int32_t *offsets, int G, int M,
-                        int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
-                        cudaStream_t stream);
+
+// Tile override set by moe_set_gemm_tile (MOE_TILE_AUTO: none).
+static std::atomic<int> g_forced_tile{MOE_TILE_AUTO};
 
 // Tile shape per call, from the mean rows per group (M / G), chosen from
 // GB300 measurements of the OLMoE- and DeepSeek-shaped layers:
-//   <= 64 rows : 128 x 128 tiles.  (The weight-row tiles of gemm_tc_dec.cu,
-//                which spend no MMA rows on empty token rows, measured equal
-//                or slower for bf16 once every stage took one copy per
-//                operand; int8 weights keep them for 8-48 rows, see
-//                pick_tile_w8.)
+//   <= 64 rows : 128 x 128 tiles.
 //   <= 128 rows: 128 x 256 tiles.
 //   more       : 256 x 256 tiles on CTA pairs (gemm_tc_pair.cu): 4-8 % faster
 //                than 128 x 256 for gate/up at 256-1024 rows per group and
 //                up to 6 % for down; at 64-128 rows they tie on gate/up and
 //                lose on down, so the pairs start above 128 rows.
-//                The 256-row token blocks of gemm_tc256.cu (a third fewer
-//                operand bytes per FLOP) measured 5-16 % slower than 128 x 256
-//                at 32-1024 rows per group once both kernels took one copy per
-//                operand per stage, so the choice never falls on them.
-// MOE_GEMM_TILE=dec16|dec32|dec64|128|256|prefill|pair (and, int8 only,
-// w8d16|w8d32|w8d64) in the environment overrides the choice.
-static int forced_tile() {
-    static const int forced = [] {
-        const char *v = getenv("MOE_GEMM_TILE");
-        if (!v) return -1;
-        if (!strcmp(v, "dec16")) return static_cast<int>(TILE_DEC16);
-        if (!strcmp(v, "dec32")) return static_cast<int>(TILE_DEC32);
-        if (!strcmp(v, "dec64")) return static_cast<int>(TILE_DEC64);
-        if (!strcmp(v, "128")) return static_cast<int>(TILE_128);
-        if (!strcmp(v, "256")) return static_cast<int>(TILE_256);
-        if (!strcmp(v, "prefill")) return static_cast<int>(TILE_PREFILL);
-        if (!strcmp(v, "pair")) return static_cast<int>(TILE_PAIR);
-        if (!strcmp(v, "w8d16")) return static_cast<int>(TILE_W8D16);
-        if (!strcmp(v, "w8d32")) return static_cast<int>(TILE_W8D32);
-        if (!strcmp(v, "w8d64")) return static_cast<int>(TILE_W8D64);
-        return -1;
-    }();
-    return forced;
-}
-
+// Two other bf16 tile kernels were measured and are not in the library:
+// weight-row tiles (the MMA's M over weight rows, N over a group's tokens),
+// equal or slower once every ring stage took one copy per operand, and
+// 256-row token blocks, 5-16 % slower than 128 x 256 at 32-1024 rows per
+// group (their 512 TMEM columns leave no second accumulator buffer).
 int pick_tile(int M, int G) {
-    if (forced_tile() >= 0) return forced_tile();
+    const int f = g_forced_tile.load(std::memory_order_relaxed);
+    if (f == MOE_TILE_128x128 || f == MOE_TILE_128x256 || f == MOE_TILE_PAIR) return f;
     const int64_t m = M, g = G;
-    return m <= 64 * g ? TILE_128 : m <= 128 * g ? TILE_256 : TILE_PAIR;
+    return m <= 64 * g ? MOE_TILE_128x128 : m <= 128 * g ? MOE_TILE_128x256 : MOE_TILE_PAIR;
 }
 
 // int8 weights, from the mean rows per group (OLMoE int8 layer on GB300, us
 // per layer; 256-row weight tiles of gemm_tc_dec_w8.cu with 16/32/64 tokens,
-// 128-row weight tiles of gemm_tc_dec.cu with 64 tokens, 256-token-row
-// tiles of gemm_tc_w8.cu):
+// 256-token-row tiles of gemm_tc_w8.cu):
 //     rows/group      1      2      8     16     24     32     48     64
 //     w8d16        99.3  119.8  123.4  162.7  188.9  231.9  295.9  383.5
 //     w8d32       105.0  125.4  127.5  127.9  132.0  173.3  197.1  242.2
 //     w8d64                                          137.7  145.9  162.8
-//     dec64       131.7  170.5  173.3  174.6  179.1  180.7  180.8  244.3
-//     256         139.8  170.9  174.6  175.3  179.1  180.9  184.8  190.9
+//     rows        139.8  170.9  174.6  175.3  179.1  180.9  184.8  190.9
 //     rows/group     96    128    192    256
 //     w8d64       215.5  260.6  346.6  439.2
-//     256         201.7  242.2  324.5  399.8
-// (the 128-row tiles with 16 and 32 tokens: 127.5 / 129.5 us at 1 row per
-// group, 168.7 / 170.5 at 8; 256-row tiles with 128 tokens and a single
-// accumulator buffer: 207 us at 64 rows, 428 at 256.)
+//     rows        201.7  242.2  324.5  399.8
+// (256-row tiles with 128 tokens and a single accumulator buffer: 207 us at
+// 64 rows, 428 at 256.)
 int pick_tile_w8(int M, int G) {
-    if (forced_tile() >= 0) return forced_tile();
+    const int f = g_forced_tile.load(std::memory_order_relaxed);
+    if (f == MOE_TILE_W8_D16 || f == MOE_TILE_W8_D32 || f == MOE_TILE_W8_D64 ||
+        f == MOE_TILE_W8_ROWS)
+        return f;
     const int64_t m = M, g = G;
-    if (m <= 10 * g) return TILE_W8D16;
-    if (m <= 24 * g) return TILE_W8D32;
-    if (m <= 64 * g) return TILE_W8D64;
-    return TILE_256;
+    if (m <= 10 * g) return MOE_TILE_W8_D16;
+    if (m <= 24 * g) return MOE_TILE_W8_D32;
+    if (m <= 64 * g) return MOE_TILE_W8_D64;
+    return MOE_TILE_W8_ROWS;
 }
 }  // namespace moe
+
+extern "C" moe_status moe_set_gemm_tile(int tile) {
+    if (tile < MOE_TILE_AUTO || tile > MOE_TILE_W8_ROWS) return MOE_ERR_INVALID_ARG;
+    moe::g_forced_tile.store(tile, std::memory_order_relaxed);
+    return MOE_OK;
+}
 
 template <bool SWIGLU>
 static moe_status launch_tc_bn(const void *act, const void *w, const int32_t *offsets, int G,
                                int M, int K, int R, int NOUT, int UP_OFF, uint16_t *out,
                                int32_t *dev_error, cudaStream_t stream) {
-    const int tile = pick_tile(M, G);
-    switch (tile) {
-        case TILE_DEC16:
-        case TILE_DEC32:
-        case TILE_DEC64:
-            return launch_dec<SWIGLU, false>(dec_tn(tile), act, w, nullptr, offsets, G, M, K, R,
-                                             NOUT, UP_OFF, out, dev_error, stream);
-        case TILE_128:
+    switch (pick_tile(M, G)) {
+        case MOE_TILE_128x128:
             return launch_tc<SWIGLU, 128>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
                                           dev_error, stream);
-        case TILE_256:
+        case MOE_TILE_128x256:
             return launch_tc<SWIGLU, 256>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
                                           dev_error, stream);
-        case TILE_PAIR:
+        default:
             return launch_tc_pair<SWIGLU>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
                                           dev_error, stream);
-        default:
-            return launch_tc256<SWIGLU>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,
-                                        stream);
     }
 }
 

@@ -1,17 +1,17 @@
 // gemm_tc_dec_w8.cu -- int8 weight-only grouped GEMM for decode-sized expert
 // groups: 256 weight rows per tile, the widened weights in tensor memory.
 //
-// The same computation as the int8 mode of gemm_tc_dec.cu ("dispatch"
-// README, phase 5a: per-channel int8 weights, fp32 scales, bf16
-// activations; "switchyard" page, 02 Kernels and dispatch: all experts in one
-// launch), D[f, j] = sum_k W_g[f, k] * X[j, k] with the weight rows as the
-// MMA's M and a block of TN token rows as its N.
+// Per-channel int8 weights with fp32 scales and bf16 activations ("dispatch"
+// README, phase 5a), all experts in one launch ("switchyard" page, 02
+// Kernels and dispatch): D[f, j] = sum_k W_g[f, k] * X[j, k] with the weight
+// rows as the MMA's M and a block of TN token rows as its N, so no MMA rows
+// go to the empty token rows of a small group.
 //
-// Why a kernel of its own: in the int8 mode of that kernel, each 64-deep
-// k-step of 8 KB of int8 weights costs the MMA-issuing thread ~0.44 us (two
-// barrier waits, four M = 128 MMAs, two commits; %globaltimer stamps at
-// every hand-off), which holds the weight stream near 3 TB/s.  Back to back
-// on one SM an M = 128, N = 16 or 32 tcgen05.mma takes ~22.5 ns and a
+// Why this shape: with 128 weight rows per tile and 64-deep k-steps, each
+// 8 KB of int8 weights cost the MMA-issuing thread ~0.44 us (two barrier
+// waits, four M = 128 MMAs, two commits; %globaltimer stamps at every
+// hand-off), which held the weight stream near 3 TB/s.  Back to back on one
+// SM an M = 128, N = 16 or 32 tcgen05.mma takes ~22.5 ns and a
 // tcgen05.commit ~23 ns (measured), so at decode-sized N the per-k-step
 // hand-offs, not the tensor core, set the pace.  Here a tile holds 256 weight
 // rows (in SwiGLU mode the gate rows of 128 features and the matching up

@@ -356,13 +356,12 @@ static moe_status launch_tc_w8(const void *act, const int8_t *q, const float *sc
                                const int32_t *offsets, int G, int M, int K, int R, int NOUT,
                                int UP_OFF, uint16_t *out, int32_t *dev_error, cudaStream_t stream) {
     const int tile = pick_tile_w8(M, G);
-    if (tile == TILE_W8D16 || tile == TILE_W8D32 || tile == TILE_W8D64)
-        return launch_dec_w8<SWIGLU>(tile == TILE_W8D16 ? 16 : tile == TILE_W8D32 ? 32 : 64, act,
-                                     q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error,
-                                     stream);
-    if (tile == TILE_DEC16 || tile == TILE_DEC32 || tile == TILE_DEC64)
-        return launch_dec<SWIGLU, true>(dec_tn(tile), act, q, scales, offsets, G, M, K, R, NOUT,
-                                        UP_OFF, out, dev_error, stream);
+    if (tile == MOE_TILE_W8_D16 || tile == MOE_TILE_W8_D32 || tile == MOE_TILE_W8_D64)
+        return launch_dec_w8<SWIGLU>(tile == MOE_TILE_W8_D16   ? 16
+                                     : tile == MOE_TILE_W8_D32 ? 32
+                                                               : 64,
+                                     act, q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out,
+                                     dev_error, stream);
     CUtensorMap tm_act, tm_act32, tm_act64, tm_act128, tm_q;
     if (!encode_bf16_2d(&tm_act, act, K, M, 16) || !encode_bf16_2d(&tm_act32, act, K, M, 32) ||
         !encode_bf16_2d(&tm_act64, act, K, M, 64) || !encode_bf16_2d(&tm_act128, act, K, M, TC_BM))

@@ -239,20 +239,10 @@ inline bool raise_smem_limit(Kernel kernel, int *done_per_device) {
     return true;
 }
 
-// Tile shapes of the grouped GEMMs (gemm_tc.cu picks one per call).
-enum {
-    TILE_DEC16 = 0, TILE_DEC32, TILE_DEC64, TILE_128, TILE_256, TILE_PREFILL, TILE_PAIR,
-    TILE_W8D16, TILE_W8D32, TILE_W8D64
-};
+// Tile shape of each grouped GEMM call (gemm_tc.cu picks one; the values
+// are moe_tile's, include/moe.h).
 int pick_tile(int M, int G);
 int pick_tile_w8(int M, int G);
-inline int dec_tn(int tile) { return tile == TILE_DEC16 ? 16 : tile == TILE_DEC32 ? 32 : 64; }
-
-// Weight-row tiles for decode-sized groups (gemm_tc_dec.cu); scales: int8 only.
-template <bool SWIGLU, bool W8>
-moe_status launch_dec(int tn, const void *tok, const void *w, const float *scales,
-                      const int32_t *offsets, int G, int M, int K, int R, int NOUT, int UP_OFF,
-                      uint16_t *out, int32_t *dev_error, cudaStream_t stream);
 
 // int8 weights, 256 weight rows x TN (16, 32 or 64) token rows (gemm_tc_dec_w8.cu).
 template <bool SWIGLU>

@@ -189,6 +189,32 @@ moe_status moe_route_permute(const float *logits, int T, int E, int S, int k, in
                              int32_t *offsets, int32_t *sorted_slot, int32_t *row_of_slot,
                              uint16_t *x_perm, int32_t *dev_error, cudaStream_t stream);
 
+/*
+ * Tile shapes of the grouped GEMM calls.  Each call picks one from the mean
+ * permuted rows per group (M / G); moe_set_gemm_tile overrides that choice
+ * for every later call in the process, so that tests can run each tile
+ * kernel on any batch and tuning can compare them.  bf16 weights:
+ * MOE_TILE_128x128 (up to 64 rows per group), MOE_TILE_128x256 (up to 128),
+ * MOE_TILE_PAIR (256 x 256 tiles on CTA pairs, above).  int8 weights:
+ * 256 weight rows x 16 / 32 / 64 tokens (MOE_TILE_W8_D16 up to 10 rows per
+ * group, _D32 up to 24, _D64 up to 64), MOE_TILE_W8_ROWS (256 token rows x
+ * 128 weight rows, above).  A forced tile of the other weight type leaves
+ * that type's choice automatic.  Not synchronised with calls in flight on
+ * other host threads; the results of every tile are within the same bounds
+ * of the exact layer.  Returns MOE_ERR_INVALID_ARG for an unknown value.
+ */
+typedef enum {
+    MOE_TILE_AUTO = -1,
+    MOE_TILE_128x128 = 0,
+    MOE_TILE_128x256 = 1,
+    MOE_TILE_PAIR = 2,
+    MOE_TILE_W8_D16 = 3,
+    MOE_TILE_W8_D32 = 4,
+    MOE_TILE_W8_D64 = 5,
+    MOE_TILE_W8_ROWS = 6
+} moe_tile;
+moe_status moe_set_gemm_tile(int tile);
+
 /* Workspace bytes of the FFN calls below: the bf16 hidden rows h [M,I]. */
 size_t moe_ffn_workspace_size(int M, int I);
 

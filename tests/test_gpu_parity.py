@@ -342,36 +342,31 @@ def test_fused_route_permute_limits_and_nan(B, L):
 
 
 @pytest.mark.parametrize("tile,case", [(t, ("deepseek", 512, "zipf")) for t in
-                                       ("dec16", "dec32", "dec64", "128", "256", "prefill", "pair")]
+                                       ("128x128", "128x256", "pair")]
                          + [("pair", ("olmoe", 2048, "uniform")), ("pair", ("olmoe", 700, "zipf"))])
 def test_gemm_tile_shapes_agree(B, L, tile, case):
-    """Every tile shape of the tcgen05 GEMM (weight-row tiles with 16/32/64-
-    token blocks, 128 x 128, 128 x 256, 256-row prefill blocks, 256 x 256
-    tiles on CTA pairs; normally chosen per call from the rows per group)
-    gives results within tolerance
-    of the oracle on a DeepSeek-shaped batch (zipf routing: group sizes from
-    a few rows to the 512-row shared experts)."""
-    import subprocess, sys, os
-    code = (
-        "import sys; sys.path.insert(0, %r)\n"
-        "import numpy as np, torch, oracle\n"
-        "from grouped_expert_gemm_moe_gb300 import workloads as W\n"
-        "from grouped_expert_gemm_moe_gb300.layer import MoELayer\n"
-        "sys.path.insert(0, %r)\n"
-        "from gpu_helpers import host_inputs, oracle_out, sample_tokens, assert_close, to_np\n"
-        "inp = W.make_layer(W.CONFIGS[%r], %d, %r, seed=0, device='cuda:0')\n"
-        "h = host_inputs(inp); sh = inp.shape\n"
-        "ly = MoELayer(sh.H, sh.E, sh.k, sh.I, sh.S, sh.renormalize, w_gu=inp.w_gu, w_down=inp.w_down, device='cuda:0')\n"
-        "out = ly.forward(inp.x, inp.logits, ffn='gemm'); ly.check()\n"
-        "tok = sample_tokens(%d)\n"
-        "_, _, y = oracle_out(inp, h, tokens=tok)\n"
-        "print(assert_close(to_np(out)[tok], y, 'bn'))\n"
-    ) % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-         os.path.dirname(os.path.abspath(__file__)), case[0], case[1], case[2], case[1])
-    env = dict(os.environ, MOE_GEMM_TILE=tile)
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                       timeout=600)
-    assert r.returncode == 0, r.stdout + r.stderr
+    """Every tile shape of the tcgen05 GEMM (128 x 128, 128 x 256, 256 x 256
+    on CTA pairs; normally chosen per call from the rows per group), forced
+    for every call, gives results within tolerance of the oracle on every
+    token of a DeepSeek-shaped batch (zipf routing: group sizes from a few
+    rows to the 512-row shared experts) and, for the pair tiles, of two
+    OLMoE-shaped batches."""
+    inp, h = layer_case(*case)
+    layer = make_layer_obj(L, inp)
+    with B.forced_gemm_tile(tile):
+        out = layer.forward(inp.x.to(DEV), inp.logits.to(DEV), ffn="gemm")
+        layer.check()
+    tok = sample_tokens(case[1])
+    _, _, y = oracle_out(inp, h, tokens=tok)
+    assert_close(to_np(out)[tok], y, f"tile {tile} {case}")
+
+
+def test_gemm_tile_override_is_validated(B):
+    for bad in (-2, 7, 100):
+        assert B._lib.moe_set_gemm_tile(bad) == 1          # MOE_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        B.moe_set_gemm_tile("dec16")
+    B.moe_set_gemm_tile("auto")
 
 
 @pytest.mark.parametrize("T,E,k,renorm", [(1, 64, 8, 0), (64, 64, 8, 0), (700, 96, 6, 1),

@@ -83,7 +83,10 @@ def test_w8_layer_matches_oracle(mods, T, routing, ffn):
                                           (144, 208, 5, 1, 2, 90)])
 def test_w8_gemm_rows_vs_oracle(mods, H, I, E, S, k, T):
     """Every permuted row of the int8 tensor-core FFN on ragged tiles."""
-    B, L = mods
+    _w8_rows_check(*mods, H, I, E, S, k, T)
+
+
+def _w8_rows_check(B, L, H, I, E, S, k, T):
     sh = W.MoEShape("t8", H=H, E=E, k=k, I=I, S=S)
     inp = W.make_layer(sh, T, "uniform", seed=5)
     q_gu, s_gu = B.moe_quantize_w8(inp.w_gu)
@@ -184,88 +187,62 @@ def test_stack_graph_replay_matches_eager(mods):
         x0.copy_(torch.randn(x0.shape, generator=g, device=DEV).to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("tile", ["dec16", "dec32", "dec64", "w8d16", "w8d32", "w8d64", "128"])
-def test_w8_gemm_tile_shapes_agree(tile):
-    """Every int8 tensor-core kernel, forced (128-row weight tiles of 16/32/64
-    tokens, 256-row weight tiles of 16/32/64 tokens, the 128-token-row kernel;
-    normally chosen by rows per group),
-    matches the oracle's int8 layer on an OLMoE-shaped T=128 zipf batch
-    (group sizes from a few rows to several dozen)."""
-    import os
-    import subprocess
-    import sys
-    here = os.path.dirname(os.path.abspath(__file__))
-    code = (
-        "import sys; sys.path.insert(0, %r); sys.path.insert(0, %r)\n"
-        "import torch, oracle\n"
-        "import __graft_entry__ as g; g.build()\n"
-        "from grouped_expert_gemm_moe_gb300 import binding as B, layer as L, workloads as W\n"
-        "import test_gpu_w8_stack as t\n"
-        "from gpu_helpers import assert_close, sample_tokens, to_np\n"
-        "layer, inp, (qg, sg, qd, sd) = t.w8_layer(B, L)\n"
-        "sh = W.OLMOE_W8\n"
-        "x, logits = t.batch(sh, 128, 'zipf', inp.w_r, 5)\n"
-        "out = layer.forward(x.to('cuda:0'), logits.to('cuda:0'), ffn='gemm'); layer.check()\n"
-        "tok = sample_tokens(128)\n"
-        "ids, w = oracle.route(logits.numpy(), sh.k, sh.renormalize)\n"
-        "y = oracle.moe_layer_w8(W.bf16_bits(x), ids, w, sh.E, sh.S, qg, sg, qd, sd, tokens=tok)\n"
-        "print(assert_close(to_np(out)[tok], y, 'w8 tile'))\n"
-    ) % (os.path.dirname(here), here)
-    env = dict(os.environ, MOE_GEMM_TILE=tile)
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                       timeout=600)
-    assert r.returncode == 0, r.stdout + r.stderr
+W8_TILES = ["w8_d16", "w8_d32", "w8_d64", "w8_rows"]
 
 
-@pytest.mark.parametrize("tile", ["w8d16", "w8d32", "w8d64", "dec16"])
-def test_w8_forced_tiles_on_ragged_shapes(tile):
+@pytest.mark.parametrize("tile", W8_TILES)
+def test_w8_gemm_tile_shapes_agree(mods, tile):
+    """Every int8 tensor-core kernel, forced for every call (256-row weight
+    tiles of 16/32/64 tokens, the 256-token-row kernel; normally chosen by
+    rows per group), matches the oracle's int8 layer on every token of an
+    OLMoE-shaped T=128 zipf batch (group sizes from a few rows to several
+    dozen)."""
+    B, L = mods
+    layer, inp, (qg, sg, qd, sd) = w8_layer(B, L)
+    sh = W.OLMOE_W8
+    x, logits = batch(sh, 128, "zipf", inp.w_r, 5)
+    with B.forced_gemm_tile(tile):
+        out = layer.forward(x.to(DEV), logits.to(DEV), ffn="gemm")
+        layer.check()
+    ids, w = oracle.route(logits.numpy(), sh.k, sh.renormalize)
+    y = oracle.moe_layer_w8(W.bf16_bits(x), ids, w, sh.E, sh.S, qg, sg, qd, sd)
+    assert_close(to_np(out), y, f"w8 tile {tile}")
+
+
+@pytest.mark.parametrize("tile", W8_TILES)
+@pytest.mark.parametrize("H,I,E,S,k,T", [(144, 208, 5, 1, 2, 300), (256, 512, 4, 0, 1, 1000),
+                                          (144, 208, 5, 1, 2, 12), (144, 208, 5, 1, 2, 40),
+                                          (144, 208, 5, 1, 2, 90)])
+def test_w8_forced_tiles_on_ragged_shapes(mods, tile, H, I, E, S, k, T):
     """The ragged-tile rows test (K not a multiple of 64, intermediate and
     hidden sizes that leave partial 128- and 256-row weight tiles, 12 to
     1000 tokens) with one int8 tile kernel forced for every call."""
-    import os
-    import subprocess
-    import sys
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, MOE_GEMM_TILE=tile)
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu",
-                        os.path.join(here, "test_gpu_w8_stack.py"), "-k", "rows_vs_oracle"],
-                       env=env, capture_output=True, text=True, timeout=900,
-                       cwd=os.path.dirname(here))
-    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
+    B, L = mods
+    with B.forced_gemm_tile(tile):
+        _w8_rows_check(B, L, H, I, E, S, k, T)
 
 
-@pytest.mark.parametrize("tile", ["w8d16", "w8d32", "w8d64", "dec64", "256"])
-def test_w8_forced_tiles_deterministic_at_prefill_size(tile):
+@pytest.mark.parametrize("tile", W8_TILES)
+def test_w8_forced_tiles_deterministic_at_prefill_size(mods, tile):
     """Each int8 tile kernel, forced, gives byte-identical FFN output (the
     permuted rows y and the hidden rows h) over three runs of an OLMoE int8
     T=2048 batch: the widened weight stages are rewritten while the next
     stages are read, so a missing ordering shows up as run-to-run changes."""
-    import os
-    import subprocess
-    import sys
-    here = os.path.dirname(os.path.abspath(__file__))
-    code = (
-        "import sys; sys.path.insert(0, %r); sys.path.insert(0, %r)\n"
-        "import torch\n"
-        "import __graft_entry__ as g; g.build()\n"
-        "from grouped_expert_gemm_moe_gb300 import binding as B, layer as L, workloads as W\n"
-        "import test_gpu_w8_stack as t\n"
-        "layer, inp, _ = t.w8_layer(B, L)\n"
-        "sh = W.OLMOE_W8\n"
-        "x, logits = t.batch(sh, 2048, 'uniform', inp.w_r, 3)\n"
-        "b = layer.buffers(2048)\n"
-        "layer.route(logits.to('cuda:0'), b); layer.permute(x.to('cuda:0'), b)\n"
-        "M = layer.rows(2048)\n"
-        "outs = []\n"
-        "for rep in range(3):\n"
-        "    b.ffn_ws.zero_(); b.y_perm.zero_()\n"
-        "    layer.ffn(b, 'gemm'); torch.cuda.synchronize(); layer.check()\n"
-        "    outs.append((b.ffn_ws[:M * sh.I * 2].clone(), b.y_perm[:M].clone()))\n"
-        "for h, y in outs[1:]:\n"
-        "    assert torch.equal(h, outs[0][0]) and torch.equal(y, outs[0][1]), 'runs differ'\n"
-        "print('deterministic')\n"
-    ) % (os.path.dirname(here), here)
-    env = dict(os.environ, MOE_GEMM_TILE=tile)
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                       timeout=600)
-    assert r.returncode == 0 and "deterministic" in r.stdout, r.stdout + r.stderr
+    B, L = mods
+    layer, inp, _ = w8_layer(B, L)
+    sh = W.OLMOE_W8
+    x, logits = batch(sh, 2048, "uniform", inp.w_r, 3)
+    b = layer.buffers(2048)
+    layer.route(logits.to(DEV), b)
+    layer.permute(x.to(DEV), b)
+    M = layer.rows(2048)
+    outs = []
+    with B.forced_gemm_tile(tile):
+        for _ in range(3):
+            b.ffn_ws.zero_()
+            b.y_perm.zero_()
+            layer.ffn(b, "gemm")
+            layer.check()
+            outs.append((b.ffn_ws[:M * sh.I * 2].clone(), b.y_perm[:M].clone()))
+    for h, y in outs[1:]:
+        assert torch.equal(h, outs[0][0]) and torch.equal(y, outs[0][1]), f"{tile}: runs differ"
