@@ -309,10 +309,9 @@ static std::atomic<int> g_forced_tile{MOE_TILE_AUTO};
 // GB300 measurements of the OLMoE- and DeepSeek-shaped layers:
 //   <= 64 rows : 128 x 128 tiles.
 //   <= 128 rows: 128 x 256 tiles.
-//   more       : 256 x 256 tiles on CTA pairs (gemm_tc_pair.cu): 4-8 % faster
-//                than 128 x 256 for gate/up at 256-1024 rows per group and
-//                up to 6 % for down; at 64-128 rows they tie on gate/up and
-//                lose on down, so the pairs start above 128 rows.
+//   more       : CTA-pair tiles of 256 weight rows x up to 256 tokens
+//                (gemm_tc_pair.cu), when K is a multiple of 64 (else 128 x
+//                256).
 // Two other bf16 tile kernels were measured and are not in the library:
 // weight-row tiles (the MMA's M over weight rows, N over a group's tokens),
 // equal or slower once every ring stage took one copy per operand, and
@@ -369,7 +368,11 @@ static moe_status launch_tc_bn(const void *act, const void *w, const int32_t *of
             return launch_tc<SWIGLU, 256>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
                                           dev_error, stream);
         default:
-            return launch_tc_pair<SWIGLU>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
+            // the pair kernel reads whole 64-deep k-blocks; other K take 128 x 256
+            if (K % TC_BK == 0)
+                return launch_tc_pair<SWIGLU>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
+                                              dev_error, stream);
+            return launch_tc<SWIGLU, 256>(act, w, offsets, G, M, K, R, NOUT, UP_OFF, out,
                                           dev_error, stream);
     }
 }

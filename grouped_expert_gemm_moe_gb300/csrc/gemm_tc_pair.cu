@@ -1,34 +1,43 @@
-// gemm_tc_pair.cu -- the grouped GEMM on CTA pairs (tcgen05 cta_group::2).
+// gemm_tc_pair.cu -- the grouped GEMM on CTA pairs (tcgen05 cta_group::2),
+// for prefill-sized expert groups.
 //
-// The same computation as gemm_tc.cu ("switchyard" page, 02 Kernels and
-// dispatch, "One launch for all experts": one launch for all experts, SwiGLU
-// fused into the gate/up epilogue), for prefill-sized groups.  Two CTAs of a
-// cluster form a pair on two SMs and share one 256 x 256 tile:
+// The same computation as gemm_tc.cu (one launch for all experts, SwiGLU in
+// the gate/up epilogue: "switchyard" page, 02 Kernels and dispatch, "One
+// launch for all experts").  Here the operands are swapped: the MMA's M is
+// 256 weight rows and its N is a block of the group's tokens,
+//     D[w, j] = sum_k W_g[w, k] * X[m0 + j, k],
+// so the tensor-core work of a tile follows the group's row count in steps
+// of 16 (a 192-row group costs 192 columns, a group's 16-row remainder 16),
+// where token rows as M padded every m-block to 256 or 128 rows: measured
+// on GB300, an M = 128 pair MMA takes as long as an M = 256 one, and the
+// padded blocks were a third of the tensor work at 256 rows per expert.
 //
-//  * CTA r (r = 0, 1 in the cluster) stages token rows m0 + 128r .. +127 of
-//    the tile (its half of A) and weight rows 128r .. 128r+127 of the tile
-//    (its half of B: in SwiGLU mode the gate rows in CTA 0 and the matching
-//    up rows in CTA 1) -- 32 KB per 64-deep k-step per SM, where a 128 x 256
-//    tile on one SM stages 48 KB for the same MMA work.  With the ring bound
-//    by operand bytes in flight per SM, that is 1.5x the MMA work per staged
-//    byte, and the 192 KB ring holds 6 stages instead of 4;
-//  * CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): the
-//    tensor cores of both SMs run it, each reading its own shared memory, and
-//    CTA r's TMEM receives rows 128r .. 128r+127 of the accumulator with all
-//    256 columns, so each CTA's epilogue finds gate and up values of its own
-//    token rows side by side, as in the one-SM kernel;
-//  * both CTAs' copies of a stage complete on CTA 0's stage barrier (CTA 0
+//  * A pair tile is (group g, n-tile of 256 weight rows, m-block of at most
+//    256 tokens).  A group's m-blocks are balanced (equal sizes rounded up
+//    to 16), so they take about equally long.
+//  * CTA r (r = 0, 1 of the cluster) stages its 128 weight rows (its half of
+//    A) and tokens m0 + r N/2 .. m0 + (r+1) N/2 - 1 (its half of B), 32 KB
+//    per 64-deep k-step.  SwiGLU: CTA r's 128 rows are 64 features' gate and
+//    up rows, in 16-row slices of 8 gate rows then the matching 8 up rows
+//    (one 4-D TMA box over the [G, 2, I, K] weights), so in TMEM a warp's 32
+//    lanes hold the gate and up values of 16 features, 8 lanes apart.
+//  * CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 16 .. 256, K = 16):
+//    the tensor cores of both SMs run it, and CTA r's TMEM receives its own
+//    128 weight rows (lanes) by the N tokens (columns).
+//  * Both CTAs' copies of a stage complete on CTA 0's stage barrier (CTA 0
 //    arms it with the bytes of both); CTA 0's MMA commits arrive on the
-//    stage-free and accumulator-full barriers of both CTAs (multicast), and
-//    both CTAs' epilogue warps arrive on CTA 0's accumulator-free barrier;
-//  * TMEM (2 x 256 columns per CTA: double-buffered accumulators) is
+//    stage-free and accumulator-full barriers of both CTAs (multicast);
+//    both CTAs' epilogue warps arrive on CTA 0's accumulator-free barrier.
+//  * Epilogue (4 warps per CTA, lane = weight row): 16 token columns at a
+//    time are read from TMEM; SwiGLU exchanges gate and up values between
+//    lanes 8 apart with one shuffle per token pair; a warp transposes its
+//    16 tokens x 16 (SwiGLU) or 32 (down) features through 1 KB of shared
+//    memory and stores whole 32- or 64-byte row segments.
+//  * TMEM: 2 x 256 columns per CTA (double-buffered accumulators),
 //    allocated and freed by one warp of each CTA together (cta_group::2).
-// The pair tile table is the one-SM table with 256-row m-blocks; a CTA whose
-// half of an m-block holds no rows of the group still stages its weight half
-// (the peer needs it) and skips its token copy; its accumulator rows are
-// never stored.  Every mbarrier wait is bounded (1 s): on running out the
-// kernel records MOE_ERR_TIMEOUT, stops issuing, drains what it can observe
-// and meets its peer at the closing cluster barrier before freeing TMEM.
+// Every mbarrier wait is bounded (1 s): on running out the kernel records
+// MOE_ERR_TIMEOUT, stops issuing, drains what it can observe and meets its
+// peer at the closing cluster barrier before freeing TMEM.
 #include <algorithm>
 
 #include "tc_common.cuh"
@@ -38,54 +47,134 @@ namespace moe {
 
 namespace {
 
-constexpr int PAIR_BM = 256;                    // token rows per pair tile
-constexpr int PAIR_BN = 256;                    // weight rows per pair tile (MMA N)
-constexpr int PAIR_A_BYTES = 128 * TC_BK * 2;   // per CTA: 128 token rows
-constexpr int PAIR_B_BYTES = 128 * TC_BK * 2;   // per CTA: 128 weight rows
+constexpr int PAIR_MAX_N = 256;                 // tokens per pair tile (MMA N)
+constexpr int PAIR_W_ROWS = 256;                // weight rows per pair tile (MMA M)
+constexpr int PAIR_KB = 2;                      // 64-deep k-blocks per stage (K = 128)
+constexpr int PAIR_A_KB_BYTES = 128 * TC_BK * 2;                // weights, one k-block, per CTA
+constexpr int PAIR_A_BYTES = PAIR_KB * PAIR_A_KB_BYTES;        // 32 KB
+constexpr int PAIR_B_BYTES = PAIR_KB * 128 * TC_BK * 2;        // tokens: up to 128 rows, 32 KB
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
-constexpr int PAIR_STAGES = (192 * 1024) / PAIR_STAGE_BYTES;   // 6
-constexpr uint32_t PAIR_TMEM_COLS = 2 * PAIR_BN;               // two accumulators
+constexpr int PAIR_STAGES = (192 * 1024) / PAIR_STAGE_BYTES;   // 3
+constexpr uint32_t PAIR_TMEM_COLS = 2 * PAIR_MAX_N;            // two accumulators
 constexpr int PAIR_BAR_BYTES = 256;
 constexpr int PAIR_EPI_WARPS = 4;
+constexpr int PAIR_STAGING_BYTES = 1024;                        // per epilogue warp
+constexpr int PAIR_XMAPS = 8;                                   // token boxes of 16 .. 128 rows
+constexpr int PAIR_MY_MAX = 128;     // a pair's tiles decoded once at the start (more: on the fly)
 
 static_assert((2 * PAIR_STAGES + 5) * 8 + 8 <= PAIR_BAR_BYTES, "barrier block");
 
 }  // namespace
 
-// SWIGLU: out = h [M, NOUT=I], weights [G*2I, K=H] (up rows at +UP_OFF = I).
-// PLAIN : out = y [M, NOUT=H], weights [G*H,  K=I].
+// A group of `rows` tokens in m-blocks of at most 256: nmb blocks of bs rows
+// (bs a multiple of 16), the last one possibly shorter, none empty.
+__device__ __forceinline__ int pair_mblocks(int rows, int &bs) {
+    const int nmb0 = (rows + PAIR_MAX_N - 1) / PAIR_MAX_N;
+    bs = nmb0 > 0 ? (((rows + nmb0 - 1) / nmb0 + 15) & ~15) : PAIR_MAX_N;
+    return nmb0 > 0 ? (rows + bs - 1) / bs : 0;
+}
+
+// The pair tile table: group g owns n_tiles * nmb(rows_g) tiles from
+// s_tile[g], n-tile major, m-block fastest.  Offsets that are negative, not
+// monotone or beyond M make the launch a no-op with a device-check fault.
+__device__ __forceinline__ void build_pair_table(const int32_t *offsets, int G, int M,
+                                                 int n_tiles, int *s_off, int *s_tile,
+                                                 int *s_total, int32_t *dev_error) {
+    const int lane = lane_id();
+    int carry = 0;
+    bool bad = false;
+    for (int base = 0; base < G; base += 32) {
+        const int g = base + lane;
+        int tiles = 0;
+        if (g < G) {
+            const int o0 = offsets[g], o1 = offsets[g + 1];
+            if (o0 < 0 || o1 < o0 || o1 > M) {
+                bad = true;
+            } else {
+                int bs;
+                tiles = pair_mblocks(o1 - o0, bs) * n_tiles;
+            }
+            s_off[g] = o0;
+            if (g == G - 1) s_off[G] = o1;
+        }
+        const int inc = warp_inclusive_scan(tiles);
+        if (g < G) s_tile[g] = carry + inc - tiles;
+        carry += __shfl_sync(FULL, inc, 31);
+    }
+    bad = __any_sync(FULL, bad);
+    if (lane == 0) {
+        s_tile[G] = carry;
+        *s_total = bad ? 0 : carry;
+        if (bad) report(dev_error, MOE_ERR_DEVICE_CHECK);
+    }
+}
+
+__device__ __forceinline__ TileInfo decode_pair_tile(int t, const int *s_tile, const int *s_off,
+                                                     int G) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tile[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.g = lo;
+    const int rows = s_off[lo + 1] - s_off[lo];
+    int bs;
+    const int nmb = pair_mblocks(rows, bs);
+    const int u = t - s_tile[lo];
+    ti.nt = u / nmb;
+    const int mb = u - ti.nt * nmb;
+    ti.m0 = s_off[lo] + mb * bs;
+    ti.nrows = min(bs, rows - mb * bs);
+    return ti;
+}
+
+// The token rows x_perm [M, K] as {64, M, K / 64} (k within a k-block, row,
+// k-block): map i loads a box of 16 (i + 1) rows and two k-blocks, which
+// land as two 128-byte-swizzled [rows][64] tiles one after the other.
+struct PairTokenMaps {
+    CUtensorMap m[PAIR_XMAPS];
+};
+
+// SWIGLU: out = h [M, NOUT = I]; weights [G, 2, I, K = H] through a 5-D map
+//         (k in block, feature % 8, gate/up plane 2g + s, feature / 8, k-block).
+// PLAIN : out = y [M, NOUT = H]; weights [G * H, K = I] through a 3-D map
+//         (k in block, row, k-block).
+// K must be a multiple of 64 (a k-block never runs into the next row).
 template <bool SWIGLU>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_act16,
-                         const __grid_constant__ CUtensorMap tm_act32,
-                         const __grid_constant__ CUtensorMap tm_act64,
-                         const __grid_constant__ CUtensorMap tm_act128,
+    tc_grouped_gemm_pair(const __grid_constant__ PairTokenMaps tm_x,
                          const __grid_constant__ CUtensorMap tm_w,
                          const int32_t *__restrict__ offsets, int G, int M, int K, int R, int NOUT,
-                         int UP_OFF, uint16_t *__restrict__ out, int32_t *dev_error) {
+                         uint16_t *__restrict__ out, int32_t *dev_error) {
     constexpr int STAGES = PAIR_STAGES;
     extern __shared__ uint8_t smem_raw[];
     // the same offset in both CTAs: the MMA addresses the peer's stages by
     // the issuing CTA's shared addresses
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * PAIR_A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * PAIR_B_BYTES);
+    uint8_t *sW = smem;                                    // A: weight rows
+    uint8_t *sX = smem + STAGES * PAIR_A_BYTES;            // B: token rows
+    uint8_t *staging = sX + STAGES * PAIR_B_BYTES;         // epilogue transposes
+    uint64_t *full = reinterpret_cast<uint64_t *>(staging + PAIR_EPI_WARPS * PAIR_STAGING_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *accf = empty + STAGES;
     uint64_t *acce = accf + 2;
     uint64_t *drain = acce + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     int *s_total = reinterpret_cast<int *>(tmem_slot + 1);
-    int *s_off = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(full) + PAIR_BAR_BYTES);
+    int4 *s_my = reinterpret_cast<int4 *>(reinterpret_cast<uint8_t *>(full) + PAIR_BAR_BYTES);
+    int *s_off = reinterpret_cast<int *>(s_my + PAIR_MY_MAX);
     int *s_tile = s_off + (G + 1);
 
     const int warp = threadIdx.x >> 5, lane = lane_id();
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
-    const int n_per_tile = SWIGLU ? PAIR_BN / 2 : PAIR_BN;
+    // output columns per pair tile: 128 features (SwiGLU) or 256 rows (down)
+    const int n_per_tile = SWIGLU ? PAIR_W_ROWS / 2 : PAIR_W_ROWS;
     const int n_tiles = (NOUT + n_per_tile - 1) / n_per_tile;
-    const int KB = (K + TC_BK - 1) / TC_BK;
+    const int KB = K / TC_BK;                            // 64-deep k-blocks
+    const int KS = (KB + PAIR_KB - 1) / PAIR_KB;         // 128-deep k-steps
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -100,17 +189,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tm_act16);
-        prefetch_tmap(&tm_act32);
-        prefetch_tmap(&tm_act64);
-        prefetch_tmap(&tm_act128);
+        for (int i = 0; i < PAIR_XMAPS; ++i) prefetch_tmap(&tm_x.m[i]);
         prefetch_tmap(&tm_w);
     }
     if (warp == 1) tmem_alloc_pair<PAIR_TMEM_COLS>(tmem_slot);
     pdl_wait();
     pdl_trigger();
-    if (warp == 2)
-        build_tile_table(offsets, G, M, n_tiles, s_off, s_tile, s_total, dev_error, PAIR_BM);
+    if (warp == 2) build_pair_table(offsets, G, M, n_tiles, s_off, s_tile, s_total, dev_error);
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();           // both CTAs' barriers exist before any remote signal
@@ -119,36 +204,53 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int total = *s_total;
     const int t_first = static_cast<int>(cluster_id_x());
     const int t_step = static_cast<int>(cluster_count_x());
+    // This pair's tiles t_first, t_first + t_step, ... decoded once: a
+    // shared-memory read by the MMA thread waits behind the MMAs it has in
+    // flight, so the per-tile binary search is kept off its path.
+    if (warp == 2)
+        for (int i = lane; i < PAIR_MY_MAX; i += 32) {
+            const int t = t_first + i * t_step;
+            if (t < total) {
+                const TileInfo ti = decode_pair_tile(t, s_tile, s_off, G);
+                s_my[i] = make_int4(ti.g, ti.nt, ti.m0, ti.nrows);
+            }
+        }
+    __syncthreads();
+    auto tile_of = [&](int i, int t) -> TileInfo {
+        if (i < PAIR_MY_MAX) {
+            const int4 v = s_my[i];
+            return TileInfo{v.x, v.y, v.z, v.w};
+        }
+        return decode_pair_tile(t, s_tile, s_off, G);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (each CTA)
         if (lane == 0) {
             // a weight tile is read once per m-block of its group, by pairs
             // running at about the same time: normal L2 priority keeps it for
-            // the later readers (evict-first measured 1-3 % slower here)
+            // the later readers
             uint64_t pol_w;
             asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol_w));
-            const uint64_t pol_a = policy_evict_last();
+            const uint64_t pol_x = policy_evict_last();   // token rows: read by every n-tile
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;     // leader: per stage ever armed / parity
             bool ok = true;
-            for (int t = t_first; t < total && ok; t += t_step) {
-                const TileInfo ti = decode_tile(t, s_tile, s_off, G, PAIR_BM);
-                const PairRows pr = pair_rows(ti.nrows);
-                const int my_rows = leader ? pr.r0 : pr.r1;
-                const int abox = abox_rows(my_rows);
-                const CUtensorMap *tm_a = abox == 16 ? &tm_act16 : abox == 32 ? &tm_act32
-                                        : abox == 64 ? &tm_act64 : &tm_act128;
+            for (int t = t_first, i = 0; t < total && ok; t += t_step, ++i) {
+                const TileInfo ti = tile_of(i, t);
+                const int half = ((ti.nrows + 15) & ~15) >> 1;      // N / 2 token rows per CTA
+                const int box = (half + 15) & ~15;                  // the same in both CTAs
+                const int my_cnt = leader ? min(ti.nrows, half) : ti.nrows - half;
+                const CUtensorMap *tm = &tm_x.m[box / 16 - 1];
                 const uint32_t bytes = static_cast<uint32_t>(
-                    (abox_rows(pr.r0) + abox_rows(pr.r1)) * TC_BK * 2 + 2 * PAIR_B_BYTES);
-                // this CTA's weight rows: in SwiGLU mode the gate rows of
-                // features f0 + 64r .. +63 and the matching up rows (one 3-D
-                // box), else rows 128r .. 128r+127 of the tile
-                const int wrow = SWIGLU ? ti.nt * n_per_tile + static_cast<int>(rank) * 64
+                    (ti.nrows > half ? 2 : 1) * box * TC_BK * 2 * PAIR_KB + 2 * PAIR_A_BYTES);
+                const int xrow = ti.m0 + static_cast<int>(rank) * half;
+                // SwiGLU: features f0 + 64r .. +63 as 8-feature slices (8 gate
+                // rows, then their 8 up rows); down: rows 128r .. +127 of the tile
+                const int wrow = SWIGLU ? (ti.nt * n_per_tile + static_cast<int>(rank) * 64) / 8
                                         : ti.g * R + ti.nt * n_per_tile + static_cast<int>(rank) * 128;
-                const int arow = ti.m0 + static_cast<int>(rank) * pr.per_cta;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int ks = 0; ks < KS; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, dev_error)) {
                         ok = false;
                         break;
@@ -159,14 +261,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     }
-                    const int kx = kb * TC_BK;
-                    if (abox > 0)
-                        tma_load_2d_pair(sA + stage * PAIR_A_BYTES, tm_a, bar0, kx, arow, pol_a);
+                    const int kb = ks * PAIR_KB;
                     if (SWIGLU)
-                        tma_load_3d_pair(sB + stage * PAIR_B_BYTES, &tm_w, bar0, kx, wrow,
-                                         2 * ti.g, pol_w);
+                        tma_load_5d_pair(sW + stage * PAIR_A_BYTES, &tm_w, bar0, 0, 0, 2 * ti.g,
+                                         wrow, kb, pol_w);
                     else
-                        tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tm_w, bar0, kx, wrow, pol_w);
+                        tma_load_3d_pair(sW + stage * PAIR_A_BYTES, &tm_w, bar0, 0, wrow, kb, pol_w);
+                    if (my_cnt > 0)
+                        tma_load_3d_pair(sX + stage * PAIR_B_BYTES, tm, bar0, 0, xrow, kb, pol_x);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -181,32 +283,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (CTA 0 only)
         if (leader && lane == 0) {
-            constexpr uint32_t idesc_full = idesc_bf16_f32(PAIR_BM, PAIR_BN);
-            constexpr uint32_t idesc_half = idesc_bf16_f32(PAIR_BM / 2, PAIR_BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = t_first; t < total && ok; t += t_step) {
-                const uint32_t idesc =
-                    decode_tile(t, s_tile, s_off, G, PAIR_BM).nrows <= 128 ? idesc_half : idesc_full;
+            const uint64_t dW = sw128_kmajor_desc(smem_u32(sW));
+            const uint64_t dX = sw128_kmajor_desc(smem_u32(sX));
+            for (int t = t_first, i = 0; t < total && ok; t += t_step, ++i) {
+                const int n = (tile_of(i, t).nrows + 15) & ~15;
+                const uint32_t idesc = idesc_bf16_f32(PAIR_W_ROWS, n);
+                // the tokens' second k-block follows the first box in the stage
+                const uint32_t xkb1 = static_cast<uint32_t>((((n >> 1) + 15) & ~15) * TC_BK * 2);
                 if (!mbar_wait_cluster(&acce[acc], acc_phase ^ 1u, dev_error)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
-                for (int kb = 0; kb < KB; ++kb) {
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_MAX_N);
+                for (int ks = 0; ks < KS; ++ks) {
                     if (!mbar_wait(&full[stage], phase, dev_error)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + stage * PAIR_A_BYTES);
-                    const uint32_t b_addr = smem_u32(sB + stage * PAIR_B_BYTES);
+                    // descriptors advance by (byte offset >> 4); +32 B per 16-deep slice
+                    const uint64_t da = dW + ((stage * PAIR_A_BYTES) >> 4);
+                    const uint64_t db = dX + ((stage * PAIR_B_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < TC_BK / 16; ++kk)
-                        tc_mma_pair(d_tmem, sw128_kmajor_desc(a_addr + kk * 32),
-                                    sw128_kmajor_desc(b_addr + kk * 32), idesc,
-                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_pair(d_tmem, da + 2 * kk, db + 2 * kk, idesc,
+                                    (ks > 0 || kk > 0) ? 1u : 0u);
+                    if (ks * PAIR_KB + 1 < KB) {
+#pragma unroll
+                        for (int kk = 0; kk < TC_BK / 16; ++kk)
+                            tc_mma_pair(d_tmem, da + ((PAIR_A_KB_BYTES >> 4) + 2 * kk),
+                                        db + ((xkb1 >> 4) + 2 * kk), idesc, 1u);
+                    }
                     tc_commit_pair_both(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -226,80 +336,75 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else {
         // ------------------------------------------------ epilogue (warps 2..5, each CTA)
         const int quarter = warp & 3;       // TMEM lanes this warp may access
-        const int row_in_tile = quarter * 32 + lane;
+        uint8_t *stg = staging + (warp - 2) * PAIR_STAGING_BYTES;
         const uint32_t acce0 = map_to_rank(smem_u32(&acce[0]), 0);
         const uint32_t acce1 = map_to_rank(smem_u32(&acce[1]), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = t_first; t < total; t += t_step) {
-            const TileInfo ti = decode_tile(t, s_tile, s_off, G, PAIR_BM);
+        for (int t = t_first, i = 0; t < total; t += t_step, ++i) {
+            const TileInfo ti = tile_of(i, t);
             if (!mbar_wait_warp(&accf[acc], acc_phase, dev_error)) break;
             tc_fence_after();
-            // Accumulator layout (per CTA, TMEM columns from tbase):
-            //   M = 256 tile: lane i = row i, columns 0..255 = the tile's 256
-            //     weight rows (SwiGLU: gate f0..63, up f0..63, gate f64..127,
-            //     up f64..127);
-            //   M = 128 tile: lane i < 64 = row i, columns 0..127 = weight rows
-            //     0..127; lane 64 + i = row i, columns 0..127 = weight rows
-            //     128..255.
-            const PairRows pr = pair_rows(ti.nrows);
-            const int my_rows = leader ? pr.r0 : pr.r1;
-            const int row = pr.half ? (row_in_tile & 63) : row_in_tile;
-            const int wpart = pr.half ? (row_in_tile >> 6) : 0;   // which half of the weight rows
-            const bool valid = row < my_rows;
-            uint16_t *orow =
-                out + static_cast<int64_t>(ti.m0 + static_cast<int>(rank) * pr.per_cta + row) *
-                          NOUT;
             const uint32_t tbase =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * PAIR_BN;
-            const int n0 = ti.nt * n_per_tile;
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * PAIR_MAX_N;
             if (SWIGLU) {
-                // features fb .. fb + nf - 1 of this thread; gate of feature
-                // fb + c at column gc(c), up at gc(c) + 64
-                const int fb = wpart * 64;
-                const int nf = pr.half ? 64 : 128;
+                // lane l: feature 16 q + 8 (l >> 4) + (l & 7) of this CTA's 64,
+                // gate if bit 3 of l is 0, else up.  Gate lanes form h for the
+                // chunk's tokens 0..7, up lanes for tokens 8..15.
+                const bool is_up = (lane >> 3) & 1;
+                const int fcol = 8 * (lane >> 4) + (lane & 7);      // feature within the warp's 16
+                const int f_warp = ti.nt * n_per_tile + static_cast<int>(rank) * 64 + 16 * quarter;
+                // read-back: lane l stores token l >> 1, features 8 (l & 1) .. +7
+                const int rt = lane >> 1, rf = 8 * (lane & 1);
+                const bool f_ok = f_warp + rf < NOUT;
 #pragma unroll 1
-                for (int c = 0; c < nf; c += 16) {
-                    const int gcol = c < 64 ? c : c + 64;
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tbase + gcol, g);
-                    tmem_ld16(tbase + gcol + 64, u);
+                for (int c0 = 0; c0 < ti.nrows; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tbase + c0, v);
                     tmem_ld_wait();
-                    const int f = n0 + fb + c;
-                    if (valid && f < NOUT) {
-                        uint32_t p[8];
+                    uint16_t *hs = reinterpret_cast<uint16_t *>(stg);     // [16 tokens][16 features]
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float h0 = silu_fast(__uint_as_float(g[2 * i])) *
-                                             __uint_as_float(u[2 * i]);
-                            const float h1 = silu_fast(__uint_as_float(g[2 * i + 1])) *
-                                             __uint_as_float(u[2 * i + 1]);
-                            p[i] = pack_bf16x2(h0, h1);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + f);
-                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                        if (f + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    for (int j = 0; j < 8; ++j) {
+                        // gate lanes send gate of tokens 8..15, up lanes up of tokens 0..7
+                        const uint32_t mine = is_up ? v[j] : v[8 + j];
+                        const float other = __uint_as_float(__shfl_xor_sync(FULL, mine, 8));
+                        const float g = is_up ? other : __uint_as_float(v[j]);
+                        const float u = is_up ? __uint_as_float(v[8 + j]) : other;
+                        const float h = silu_fast(g) * u;
+                        hs[(8 * is_up + j) * 16 + fcol] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
                     }
+                    __syncwarp();
+                    const uint4 val = *reinterpret_cast<const uint4 *>(hs + rt * 16 + rf);
+                    if (c0 + rt < ti.nrows && f_ok)
+                        *reinterpret_cast<uint4 *>(
+                            out + static_cast<int64_t>(ti.m0 + c0 + rt) * NOUT + f_warp + rf) = val;
+                    __syncwarp();
                 }
             } else {
-                const int cb = wpart * 128;
-                const int nc = pr.half ? 128 : PAIR_BN;
+                // lane l: output row n0 + 128 r + 32 q + l
+                const int n_warp = ti.nt * n_per_tile + static_cast<int>(rank) * 128 + 32 * quarter;
 #pragma unroll 1
-                for (int c = 0; c < nc; c += 16) {
+                for (int c0 = 0; c0 < ti.nrows; c0 += 16) {
                     uint32_t v[16];
-                    tmem_ld16(tbase + c, v);
+                    tmem_ld16(tbase + c0, v);
                     tmem_ld_wait();
-                    const int o = n0 + cb + c;
-                    if (valid && o < NOUT) {
-                        uint32_t p[8];
+                    uint16_t *ys = reinterpret_cast<uint16_t *>(stg);     // [16 tokens][32 rows]
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            p[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
-                                               __uint_as_float(v[2 * i + 1]));
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + o);
-                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                        if (o + 8 < NOUT) dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    for (int j = 0; j < 16; ++j)
+                        ys[j * 32 + lane] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int id = lane + 32 * i;            // 64 chunks of 16 B
+                        const int rt = id >> 2, rf = 8 * (id & 3);
+                        const uint4 val = *reinterpret_cast<const uint4 *>(ys + rt * 32 + rf);
+                        if (c0 + rt < ti.nrows && n_warp + rf < NOUT)
+                            *reinterpret_cast<uint4 *>(
+                                out + static_cast<int64_t>(ti.m0 + c0 + rt) * NOUT + n_warp + rf) =
+                                val;
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -324,20 +429,56 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // ------------------------------------------------------------------ host
 
 static size_t pair_smem_bytes(int G) {
-    return 1024 + static_cast<size_t>(PAIR_STAGES) * PAIR_STAGE_BYTES + PAIR_BAR_BYTES +
+    return 1024 + static_cast<size_t>(PAIR_STAGES) * PAIR_STAGE_BYTES +
+           PAIR_EPI_WARPS * PAIR_STAGING_BYTES + PAIR_BAR_BYTES + PAIR_MY_MAX * sizeof(int4) +
            2 * static_cast<size_t>(G + 1) * sizeof(int);
+}
+
+// Maps of the pair kernel.  Every one views K as (k within a 64-element
+// k-block, ..., k-block) so that a box brings two k-blocks (K % 64 == 0).
+//   tokens  x_perm [M, K]          -> {64, M, K/64}, box {64, rows, 2};
+//   gate/up w_gu [G, 2, I, K]      -> {64, 8, 2G, I/8, K/64}: (k, feature % 8,
+//           plane 2g + s with s = 0 gate / 1 up, feature / 8, k-block), box
+//           {64, 8, 2, 8, 2} = 64 features as 8 slices of [8 gate][8 up] rows;
+//   down    w_down [G * H, K]      -> {64, G H, K/64}, box {64, 128, 2}.
+// 128-byte swizzle (each box row is 64 bf16 = 128 bytes).
+static bool encode_pair_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                            const cuuint64_t *strides, const cuuint32_t *box) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool SWIGLU>
 moe_status launch_tc_pair(const void *act, const void *w, const int32_t *offsets, int G, int M,
                           int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,
                           cudaStream_t stream) {
-    CUtensorMap tm_act16, tm_act32, tm_act64, tm_act128, tm_w;
-    if (!encode_bf16_2d(&tm_act16, act, K, M, 16) || !encode_bf16_2d(&tm_act32, act, K, M, 32) ||
-        !encode_bf16_2d(&tm_act64, act, K, M, 64) || !encode_bf16_2d(&tm_act128, act, K, M, 128) ||
-        !(SWIGLU ? encode_gate_up_3d(&tm_w, w, K, UP_OFF, G, 64)
-                 : encode_bf16_2d(&tm_w, w, K, static_cast<uint64_t>(G) * R, 128)))
-        return MOE_ERR_CUDA;
+    (void)UP_OFF;   // SwiGLU: up rows are at +I, which the 5-D map encodes
+    if (K % TC_BK != 0 || NOUT % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    const uint64_t K64 = static_cast<uint64_t>(K) / TC_BK;
+    PairTokenMaps tm_x;
+    for (int i = 0; i < PAIR_XMAPS; ++i) {
+        const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), K64};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(16 * (i + 1)), 2};
+        if (!encode_pair_map(&tm_x.m[i], act, 3, dims, strides, box)) return MOE_ERR_CUDA;
+    }
+    CUtensorMap tm_w;
+    if (SWIGLU) {
+        const uint64_t I = static_cast<uint64_t>(NOUT);
+        const cuuint64_t dims[5] = {64, 8, 2 * static_cast<cuuint64_t>(G), I / 8, K64};
+        const cuuint64_t strides[4] = {static_cast<cuuint64_t>(K) * 2, I * K * 2, 8ull * K * 2, 128};
+        const cuuint32_t box[5] = {64, 8, 2, 8, 2};
+        if (!encode_pair_map(&tm_w, w, 5, dims, strides, box)) return MOE_ERR_CUDA;
+    } else {
+        const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(G) * R, K64};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+        const cuuint32_t box[3] = {64, 128, 2};
+        if (!encode_pair_map(&tm_w, w, 3, dims, strides, box)) return MOE_ERR_CUDA;
+    }
     const size_t smem = pair_smem_bytes(G);
     if (smem > static_cast<size_t>(max_smem_optin())) return MOE_ERR_UNSUPPORTED;
     static int attr_done[64] = {0};
@@ -371,8 +512,8 @@ moe_status launch_tc_pair(const void *act, const void *w, const int32_t *offsets
     }
     cfg.gridDim = dim3(2 * pairs_per_device[dev]);
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    cudaLaunchKernelEx(&cfg, tc_grouped_gemm_pair<SWIGLU>, tm_act16, tm_act32, tm_act64,
-                       tm_act128, tm_w, offsets, G, M, K, R, NOUT, UP_OFF, out, dev_error);
+    cudaLaunchKernelEx(&cfg, tc_grouped_gemm_pair<SWIGLU>, tm_x, tm_w, offsets, G, M, K, R, NOUT,
+                       out, dev_error);
     return launch_status();
 }
 

@@ -1,7 +1,6 @@
 // tc_pair.cuh -- CTA-pair (cluster of 2, tcgen05 cta_group::2) pieces shared
 // by the pair grouped GEMMs: cluster ids, cross-CTA barrier signals, TMA
-// loads that complete on the pair's CTA 0 barrier, pair MMAs and commits,
-// and the row split of a pair tile.
+// loads that complete on the pair's CTA 0 barrier, pair MMAs and commits.
 #pragma once
 
 #include "tc_common.cuh"
@@ -97,21 +96,28 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
-// Rows of a pair tile in CTA r: a tile of more than 128 rows is an M = 256
-// MMA with 128 rows per CTA; a group's last m-block of at most 128 rows is
-// an M = 128 MMA with 64 rows per CTA (half the tensor work).
-struct PairRows {
-    bool half;
-    int r0, r1;       // rows in CTA 0 / CTA 1
-    int per_cta;      // 128 or 64
-};
-__device__ __forceinline__ PairRows pair_rows(int nrows) {
-    PairRows p;
-    p.half = nrows <= 128;
-    p.per_cta = p.half ? 64 : 128;
-    p.r0 = min(nrows, p.per_cta);
-    p.r1 = nrows - p.r0;
-    return p;
+// The same for a 4-D box (x = k, then y, z, w).
+__device__ __forceinline__ void tma_load_4d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int x, int y, int z, int w,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster),
+        "l"(policy)
+        : "memory");
+}
+
+// The same for a 5-D box (x = k, then y, z, w, v).
+__device__ __forceinline__ void tma_load_5d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int x, int y, int z, int w,
+                                                 int v, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v),
+        "r"(bar_cluster), "l"(policy)
+        : "memory");
 }
 
 template <uint32_t NCOLS>
