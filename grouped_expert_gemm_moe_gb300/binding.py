@@ -62,6 +62,7 @@ _SIGS = {
     "moe_copy": ([P, P, SZ, P], I),
     "moe_selftest_bounded_wait": ([I, I, ctypes.c_uint64, P, P, P], I),
     "moe_set_gemm_tile": ([I], I),
+    "moe_ep_plan": ([P, I, I, I, P, P, P, P, P, P, P, P], I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -487,3 +488,27 @@ class forced_gemm_tile:
     def __exit__(self, *exc):
         moe_set_gemm_tile("auto")
         return False
+
+
+def moe_ep_plan(counts, rank: int):
+    """Expert-parallel exchange plan of `rank` (host, numpy).  counts: int
+    array [W, E] of every rank's rows per routed expert.  Returns a dict of
+    numpy arrays: send_offset, send_count, recv_offset, recv_count [W];
+    seg_src, seg_dst, seg_len [W * E/W]; local_offsets [E/W + 1]."""
+    import numpy as np
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    if c.ndim != 2:
+        raise ValueError("moe_ep_plan: counts must be [W, E]")
+    W, E = c.shape
+    EL = E // W if W > 0 else 0
+    out = {k: np.zeros(W, np.int64) for k in ("send_offset", "send_count", "recv_offset",
+                                               "recv_count")}
+    for k in ("seg_src", "seg_dst", "seg_len"):
+        out[k] = np.zeros(max(W * EL, 1), np.int64)
+    out["local_offsets"] = np.zeros(EL + 1, np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _ok(_lib.moe_ep_plan(p(c), W, E, int(rank), p(out["send_offset"]), p(out["send_count"]),
+                         p(out["recv_offset"]), p(out["recv_count"]), p(out["seg_src"]),
+                         p(out["seg_dst"]), p(out["seg_len"]), p(out["local_offsets"])),
+        "moe_ep_plan")
+    return out

@@ -406,6 +406,40 @@ moe_status moe_quantize_w8(const uint16_t *w_host, int64_t rows, int64_t K, int8
                            float *scale_host);
 
 /*
+ * moe_ep_plan -- host-side exchange plan for expert parallelism over W
+ * ranks (the "switchyard" page, Expert parallelism from the kernels up and
+ * Peer-to-peer dispatch: each GPU owns part of every layer's experts, rows
+ * travel to their expert's GPU after the sort and come back before the
+ * combine, and the output equals one GPU's).  Rank p owns the routed
+ * experts [p E/W, (p+1) E/W) (E % W == 0); shared experts are replicated
+ * and their rows never move.  No device work and no communication: the
+ * caller moves the rows (peer copies, a collective) as the plan says.
+ *   counts: [W][E] int32, host: counts[r*E + e] = rows rank r routed to
+ *           expert e (the differences of rank r's moe_permute offsets),
+ *           gathered from every rank by the caller.
+ *   send_offset/send_count [W]: rows [send_offset[p], +send_count[p]) of
+ *           this rank's x_perm go to rank p (contiguous: the rows are sorted
+ *           by expert); the results come back to the same range of y_perm.
+ *   recv_offset/recv_count [W]: rank p's rows land at recv_offset[p] of a
+ *           source-major receive buffer of sum(recv_count) rows.
+ *   seg_src/seg_dst/seg_len [W * E/W]: segment (p, j) moves seg_len rows
+ *           from row seg_src of the receive buffer to row seg_dst of the
+ *           expert-major FFN input (the reverse moves bring the FFN output
+ *           back to source-major order for the return trip).
+ *   local_offsets [E/W + 1] int32: the offsets table of the expert-major
+ *           rows for the grouped FFN over this rank's experts (append the
+ *           rank's own shared rows after it for G = E/W + S groups).
+ * Errors: MOE_ERR_INVALID_ARG for NULL pointers, W < 1, E % W != 0, a rank
+ * outside [0, W) or a negative count; MOE_ERR_UNSUPPORTED when the
+ * received rows exceed 2^31 - 1.  Nothing is written on error paths that
+ * fail the argument checks.
+ */
+moe_status moe_ep_plan(const int32_t *counts, int W, int E, int rank, int64_t *send_offset,
+                       int64_t *send_count, int64_t *recv_offset, int64_t *recv_count,
+                       int64_t *seg_src, int64_t *seg_dst, int64_t *seg_len,
+                       int32_t *local_offsets);
+
+/*
  * moe_selftest_bounded_wait -- runs one of the library's bounded device
  * waits, with a short limit, on a condition that is met (satisfiable != 0)
  * or never met, so that a test can see the failure-detection path work
