@@ -464,7 +464,7 @@ def moe_selftest_bounded_wait(kind: int, satisfiable: bool, limit_ns: int,
 
 # moe_tile values of include/moe.h
 GEMM_TILES = {"auto": -1, "128x128": 0, "128x256": 1, "pair": 2, "w8_d16": 3, "w8_d32": 4,
-              "w8_d64": 5, "w8_rows": 6}
+              "w8_d64": 5, "w8_rows": 6, "w8_pair": 7}
 
 
 def moe_set_gemm_tile(tile: str = "auto") -> None:

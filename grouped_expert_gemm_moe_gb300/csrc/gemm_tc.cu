@@ -326,7 +326,8 @@ int pick_tile(int M, int G) {
 
 // int8 weights, from the mean rows per group (OLMoE int8 layer on GB300, us
 // per layer; 256-row weight tiles of gemm_tc_dec_w8.cu with 16/32/64 tokens,
-// 256-token-row tiles of gemm_tc_w8.cu):
+// 128-token-row tiles of gemm_tc_w8.cu; above 64 rows per group the CTA-pair
+// tiles of gemm_tc_pair_w8.cu take over):
 //     rows/group      1      2      8     16     24     32     48     64
 //     w8d16        99.3  119.8  123.4  162.7  188.9  231.9  295.9  383.5
 //     w8d32       105.0  125.4  127.5  127.9  132.0  173.3  197.1  242.2
@@ -340,18 +341,18 @@ int pick_tile(int M, int G) {
 int pick_tile_w8(int M, int G) {
     const int f = g_forced_tile.load(std::memory_order_relaxed);
     if (f == MOE_TILE_W8_D16 || f == MOE_TILE_W8_D32 || f == MOE_TILE_W8_D64 ||
-        f == MOE_TILE_W8_ROWS)
+        f == MOE_TILE_W8_ROWS || f == MOE_TILE_W8_PAIR)
         return f;
     const int64_t m = M, g = G;
     if (m <= 10 * g) return MOE_TILE_W8_D16;
     if (m <= 24 * g) return MOE_TILE_W8_D32;
     if (m <= 64 * g) return MOE_TILE_W8_D64;
-    return MOE_TILE_W8_ROWS;
+    return MOE_TILE_W8_PAIR;
 }
 }  // namespace moe
 
 extern "C" moe_status moe_set_gemm_tile(int tile) {
-    if (tile < MOE_TILE_AUTO || tile > MOE_TILE_W8_ROWS) return MOE_ERR_INVALID_ARG;
+    if (tile < MOE_TILE_AUTO || tile > MOE_TILE_W8_PAIR) return MOE_ERR_INVALID_ARG;
     moe::g_forced_tile.store(tile, std::memory_order_relaxed);
     return MOE_OK;
 }

@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t idesc = idesc_bf16_f32(PAIR_W_ROWS, n);
                 // the tokens' second k-block follows the first box in the stage
                 const uint32_t xkb1 = static_cast<uint32_t>((((n >> 1) + 15) & ~15) * TC_BK * 2);
-                if (!mbar_wait_cluster(&acce[acc], acc_phase ^ 1u, dev_error)) break;
+                if (!mbar_wait(&acce[acc], acc_phase ^ 1u, dev_error)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_MAX_N);
                 for (int ks = 0; ks < KS; ++ks) {

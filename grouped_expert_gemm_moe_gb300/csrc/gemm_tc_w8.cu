@@ -356,6 +356,10 @@ static moe_status launch_tc_w8(const void *act, const int8_t *q, const float *sc
                                const int32_t *offsets, int G, int M, int K, int R, int NOUT,
                                int UP_OFF, uint16_t *out, int32_t *dev_error, cudaStream_t stream) {
     const int tile = pick_tile_w8(M, G);
+    // CTA pairs read whole 64-deep k-blocks; other K take the token-row tiles
+    if (tile == MOE_TILE_W8_PAIR && K % TC_BK == 0)
+        return launch_tc_pair_w8<SWIGLU>(act, q, scales, offsets, G, M, K, R, NOUT, UP_OFF, out,
+                                         dev_error, stream);
     if (tile == MOE_TILE_W8_D16 || tile == MOE_TILE_W8_D32 || tile == MOE_TILE_W8_D64)
         return launch_dec_w8<SWIGLU>(tile == MOE_TILE_W8_D16   ? 16
                                      : tile == MOE_TILE_W8_D32 ? 32

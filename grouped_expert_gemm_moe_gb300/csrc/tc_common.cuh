@@ -250,7 +250,14 @@ moe_status launch_dec_w8(int tn, const void *tok, const void *q, const float *sc
                          const int32_t *offsets, int G, int M, int K, int R, int NOUT, int UP_OFF,
                          uint16_t *out, int32_t *dev_error, cudaStream_t stream);
 
-// 256 x 256 tiles on CTA pairs (gemm_tc_pair.cu).
+// int8 weights on CTA pairs: 256 weight rows (widened into TMEM) x up to
+// 192 tokens (gemm_tc_pair_w8.cu).  K % 64 == 0, else MOE_ERR_UNSUPPORTED.
+template <bool SWIGLU>
+moe_status launch_tc_pair_w8(const void *act, const int8_t *q, const float *scales,
+                             const int32_t *offsets, int G, int M, int K, int R, int NOUT,
+                             int UP_OFF, uint16_t *out, int32_t *dev_error, cudaStream_t stream);
+
+// 256 weight rows x up to 256 tokens on CTA pairs (gemm_tc_pair.cu).
 template <bool SWIGLU>
 moe_status launch_tc_pair(const void *act, const void *w, const int32_t *offsets, int G, int M,
                           int K, int R, int NOUT, int UP_OFF, uint16_t *out, int32_t *dev_error,

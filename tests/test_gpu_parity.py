@@ -362,7 +362,7 @@ def test_gemm_tile_shapes_agree(B, L, tile, case):
 
 
 def test_gemm_tile_override_is_validated(B):
-    for bad in (-2, 7, 100):
+    for bad in (-2, 8, 100):
         assert B._lib.moe_set_gemm_tile(bad) == 1          # MOE_ERR_INVALID_ARG
     with pytest.raises(ValueError):
         B.moe_set_gemm_tile("dec16")

@@ -231,7 +231,7 @@ def test_stack_graph_replay_matches_eager(mods):
         x0.copy_(torch.randn(x0.shape, generator=g, device=DEV).to(torch.bfloat16))
 
 
-W8_TILES = ["w8_d16", "w8_d32", "w8_d64", "w8_rows"]
+W8_TILES = ["w8_d16", "w8_d32", "w8_d64", "w8_rows", "w8_pair"]
 
 
 @pytest.mark.parametrize("tile", W8_TILES)
