@@ -324,20 +324,20 @@ int pick_tile(int M, int G) {
     return m <= 64 * g ? MOE_TILE_128x128 : m <= 128 * g ? MOE_TILE_128x256 : MOE_TILE_PAIR;
 }
 
-// int8 weights, from the mean rows per group (OLMoE int8 layer on GB300, us
-// per layer; 256-row weight tiles of gemm_tc_dec_w8.cu with 16/32/64 tokens,
-// 128-token-row tiles of gemm_tc_w8.cu; above 64 rows per group the CTA-pair
-// tiles of gemm_tc_pair_w8.cu take over):
-//     rows/group      1      2      8     16     24     32     48     64
-//     w8d16        99.3  119.8  123.4  162.7  188.9  231.9  295.9  383.5
-//     w8d32       105.0  125.4  127.5  127.9  132.0  173.3  197.1  242.2
-//     w8d64                                          137.7  145.9  162.8
-//     rows        139.8  170.9  174.6  175.3  179.1  180.9  184.8  190.9
-//     rows/group     96    128    192    256
-//     w8d64       215.5  260.6  346.6  439.2
-//     rows        201.7  242.2  324.5  399.8
-// (256-row tiles with 128 tokens and a single accumulator buffer: 207 us at
-// 64 rows, 428 at 256.)
+// int8 weights, from the mean rows per group (int8 layers on GB300, us per
+// layer; 256-row weight tiles of gemm_tc_dec_w8.cu with 16/32/64 tokens, the
+// 128-token-row tiles of gemm_tc_w8.cu, the CTA-pair tiles of
+// gemm_tc_pair_w8.cu):
+//     OLMoE rows/group      1      2      8     16     24     32     64    128    256
+//     w8d16              99.3  119.8  123.4  162.7  188.9
+//     w8d32             105.0  125.4  127.5  127.9  132.0  173.3
+//     w8d64                                                138.4  185.5
+//     rows              139.8  170.9  174.6  175.3  179.1  181.4  191.6  241.3  403.1
+//     pair                                                 144.5  149.6  163.0  281.7
+//     DeepSeek (2 shared experts of T rows each) at 31 / 62 / 124 / 252 rows per
+//     group: w8d64 179.3 / 193.7, pair 195.7 / 207.0 / 222.3 / 330.8, rows
+//     222.3 / 249.0 / 285.8 / 521.3.
+// The pair tile takes over at 64 rows per group on average.
 int pick_tile_w8(int M, int G) {
     const int f = g_forced_tile.load(std::memory_order_relaxed);
     if (f == MOE_TILE_W8_D16 || f == MOE_TILE_W8_D32 || f == MOE_TILE_W8_D64 ||
@@ -346,7 +346,7 @@ int pick_tile_w8(int M, int G) {
     const int64_t m = M, g = G;
     if (m <= 10 * g) return MOE_TILE_W8_D16;
     if (m <= 24 * g) return MOE_TILE_W8_D32;
-    if (m <= 64 * g) return MOE_TILE_W8_D64;
+    if (m < 64 * g) return MOE_TILE_W8_D64;
     return MOE_TILE_W8_PAIR;
 }
 }  // namespace moe

@@ -15,8 +15,10 @@
 //    memory, completing on its own barrier;
 //  * warps 7-14 (each CTA): two converter groups of 4 warps take k-steps in
 //    turn; thread = TMEM lane = one weight row: it reads the row's 128 int8,
-//    releases the raw stage, widens them to bf16 (exact) and writes them with
-//    tcgen05.st into its group's A stage; CTA 0's converters also wait for
+//    releases the raw stage, widens them to bf16 (exact) in registers, and
+//    only then waits for its group's A stage and writes them there with
+//    tcgen05.st, so that between the tensor core's release of a stage and
+//    its refill lie two stores; CTA 0's converters also wait for
 //    the k-step's token stage, so the MMA thread waits on one barrier per 8
 //    MMAs; CTA 1's converters signal CTA 0's barrier across the cluster;
 //  * warp 0 (each CTA) brings the CTA's half of the tokens (two k-blocks per
@@ -56,21 +58,23 @@ constexpr int PW_RAW_BYTES = PW_KB * 128 * TC_BK;            // 128 rows x 128 i
 constexpr int PW_TOK_BYTES = PW_KB * (PW_MAX_N / 2) * TC_BK * 2;   // 96 rows: 24 KB
 constexpr int PW_RAW_STAGES = 6;                // a multiple of PW_NG
 constexpr int PW_TOK_STAGES = 4;                // a multiple of PW_NG
-constexpr int PW_NG = 2;                        // converter groups (= A stages)
+constexpr int PW_NG = 2;                        // converter groups
+constexpr int PW_A_STAGES = 2;                  // A stages, a multiple of PW_NG
 constexpr uint32_t PW_A_COL0 = 2 * PW_MAX_N;   // A stages after the two accumulators
 constexpr uint32_t PW_A_COLS = 32 * PW_KB;      // 128 bf16 per lane = 64 columns
 constexpr uint32_t PW_TMEM_COLS = 512;
 constexpr int PW_BAR_BYTES = 512;
 constexpr int PW_EPI_WARPS = 4;
 constexpr int PW_STAGING_BYTES = 1024;
-constexpr int PW_XMAPS = 6;                     // token boxes of 16 .. 96 rows
+constexpr int PW_XMAPS = PW_MAX_N / 32;          // token boxes of 16 .. 96 rows
 constexpr int PW_MY_MAX = 128;
 constexpr int PW_THREADS = (7 + 4 * PW_NG) * 32;   // 15 warps
 
-static_assert(PW_RAW_STAGES % PW_NG == 0 && PW_TOK_STAGES % PW_NG == 0,
+static_assert(PW_RAW_STAGES % PW_NG == 0 && PW_TOK_STAGES % PW_NG == 0 &&
+                  PW_A_STAGES % PW_NG == 0,
               "each ring stage must belong to one converter group");
-static_assert(PW_A_COL0 + PW_NG * PW_A_COLS <= PW_TMEM_COLS, "tensor-memory columns");
-static_assert((2 * (PW_RAW_STAGES + PW_TOK_STAGES + PW_NG) + 5) * 8 + 8 <= PW_BAR_BYTES,
+static_assert(PW_A_COL0 + PW_A_STAGES * PW_A_COLS <= PW_TMEM_COLS, "tensor-memory columns");
+static_assert((2 * (PW_RAW_STAGES + PW_TOK_STAGES + PW_A_STAGES) + 5) * 8 + 8 <= PW_BAR_BYTES,
               "barrier block");
 
 // D (+)= A[tmem] * B[smem]^T on the CTA pair (A: each CTA's 128 rows at the
@@ -192,8 +196,8 @@ __global__ void __launch_bounds__(PW_THREADS, 1)
     uint64_t *q_full = b_empty + PW_TOK_STAGES;  // own raw copy landed
     uint64_t *q_empty = q_full + PW_RAW_STAGES;  // own raw stage read (one arrival per warp)
     uint64_t *a_full = q_empty + PW_RAW_STAGES;  // CTA 0: A stage written in both CTAs
-    uint64_t *a_empty = a_full + PW_NG;          // both CTAs: MMA commit (multicast)
-    uint64_t *accf = a_empty + PW_NG;
+    uint64_t *a_empty = a_full + PW_A_STAGES;    // both CTAs: MMA commit (multicast)
+    uint64_t *accf = a_empty + PW_A_STAGES;
     uint64_t *acce = accf + 2;
     uint64_t *drain = acce + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(PW_THREADS, 1)
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 4);               // the group's 4 warps
         }
-        for (int i = 0; i < PW_NG; ++i) {
+        for (int i = 0; i < PW_A_STAGES; ++i) {
             mbar_init(&a_full[i], 2 * 4);            // the group's warps of both CTAs
             mbar_init(&a_empty[i], 1);
         }
@@ -344,10 +348,11 @@ __global__ void __launch_bounds__(PW_THREADS, 1)
         for (int t = t_first; t < total && ok; t += t_step) {
             for (int ks = 0; ks < KS; ++ks, ++seq) {
                 if (seq % PW_NG != grp) continue;
-                const int r = seq % PW_RAW_STAGES, tb = seq % PW_TOK_STAGES, s = grp;
+                const int r = seq % PW_RAW_STAGES, tb = seq % PW_TOK_STAGES;
+                const int s = seq % PW_A_STAGES;
                 const uint32_t rph = (seq / PW_RAW_STAGES) & 1;
                 const uint32_t tph = (seq / PW_TOK_STAGES) & 1;
-                const uint32_t aph = (seq / PW_NG) & 1;
+                const uint32_t aph = (seq / PW_A_STAGES) & 1;
                 if (!mbar_wait_warp(&q_full[r], rph, dev_error)) { ok = false; break; }
                 uint4 v[4 * PW_KB];
 #pragma unroll
@@ -358,22 +363,23 @@ __global__ void __launch_bounds__(PW_THREADS, 1)
                 const uint32_t done = loads_done(v);     // 0, once the loads have landed
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&q_empty[r + done]);
-                if (!mbar_wait_warp(&a_empty[s], aph ^ 1u, dev_error)) { ok = false; break; }
-                tc_fence_after();
+                uint32_t a[PW_KB][32];
 #pragma unroll
-                for (int kb = 0; kb < PW_KB; ++kb) {
-                    uint32_t a[32];
+                for (int kb = 0; kb < PW_KB; ++kb)
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
                         uint4 lo, hi;
                         widen16(v[4 * kb + p], lo, hi);
-                        a[8 * p + 0] = lo.x; a[8 * p + 1] = lo.y; a[8 * p + 2] = lo.z;
-                        a[8 * p + 3] = lo.w; a[8 * p + 4] = hi.x; a[8 * p + 5] = hi.y;
-                        a[8 * p + 6] = hi.z; a[8 * p + 7] = hi.w;
+                        a[kb][8 * p + 0] = lo.x; a[kb][8 * p + 1] = lo.y; a[kb][8 * p + 2] = lo.z;
+                        a[kb][8 * p + 3] = lo.w; a[kb][8 * p + 4] = hi.x; a[kb][8 * p + 5] = hi.y;
+                        a[kb][8 * p + 6] = hi.z; a[kb][8 * p + 7] = hi.w;
                     }
+                if (!mbar_wait_warp(&a_empty[s], aph ^ 1u, dev_error)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kb = 0; kb < PW_KB; ++kb)
                     tmem_st32_pw(a_lane + static_cast<uint32_t>(s) * PW_A_COLS +
-                                     static_cast<uint32_t>(kb * 32), a);
-                }
+                                     static_cast<uint32_t>(kb * 32), a[kb]);
                 tmem_st_wait_pw();
                 // CTA 0's converters also hold the signal until the k-step's
                 // token stage (both CTAs' copies) has landed, so the MMA
@@ -399,8 +405,8 @@ __global__ void __launch_bounds__(PW_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PW_MAX_N);
                 for (int ks = 0; ks < KS; ++ks, ++seq) {
-                    const int s = seq % PW_NG;
-                    if (!mbar_wait(&a_full[s], (seq / PW_NG) & 1, dev_error)) {
+                    const int s = seq % PW_A_STAGES;
+                    if (!mbar_wait(&a_full[s], (seq / PW_A_STAGES) & 1, dev_error)) {
                         ok = false;
                         break;
                     }
