@@ -22,10 +22,10 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(
     int S, int H, const uint16_t *residual, uint16_t *out, int32_t *dev_error) {
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.y;
+    const int t = blockIdx.y + blockIdx.z * gridDim.y;   // tokens over grid y and z
     const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * CB_CPT;   // first chunk
     const int chunks = H / 8;
-    if (c0 >= chunks) return;
+    if (t >= T || c0 >= chunks) return;
     const int64_t n = static_cast<int64_t>(T) * k;
     // shared rows follow the routed rows: at n (dropless) or after the
     // served routed rows (capacity-limited permute: offsets[E])
@@ -132,11 +132,12 @@ static moe_status combine_impl(const uint16_t *y_perm, const int32_t *row_of_slo
     if (M * H >= (1ll << 31) || T > 65535 * 64) return MOE_ERR_UNSUPPORTED;
     if (H % 8 != 0 || !aligned16(y_perm) || !aligned16(out) || (residual && !aligned16(residual)))
         return MOE_ERR_ALIGNMENT;
-    if (T > 65535) return MOE_ERR_UNSUPPORTED;   // grid.y limit
     const int chunks = H / 8;
     const int per_thread = (chunks + CB_CPT - 1) / CB_CPT;
     const int threads = per_thread >= 256 ? 256 : ((per_thread + 31) / 32) * 32;
-    dim3 grid((per_thread + threads - 1) / threads, T);
+    // tokens over grid y (at most 65535) and z
+    const int ty = T < 65535 ? T : 65535;
+    dim3 grid((per_thread + threads - 1) / threads, ty, (T + ty - 1) / ty);
     launch(combine_kernel, grid, threads, 0, stream, y_perm, row_of_slot, topk_w, offsets, E, T, k,
            S, H, residual, out, dev_error);
     return launch_status();
