@@ -15,8 +15,11 @@
 //   warps 2-5   epilogue: accumulator * per-row scale (= sum x*q*scale, the
 //               dequantised product), then SwiGLU or a plain bf16 store.
 //
-// Groups of up to 64 rows go to the 256-row weight tiles of gemm_tc_dec_w8.cu
-// instead (the weights as the MMA's M, widened into tensor memory).
+// Groups of fewer than 64 rows on average go to the 256-row weight tiles of
+// gemm_tc_dec_w8.cu, larger ones to the CTA-pair tiles of gemm_tc_pair_w8.cu
+// (both with the weights as the MMA's M, widened into tensor memory); these
+// token-row tiles run when K is not a multiple of 64 (the other kernels copy
+// whole 64-deep k-blocks) or when forced with moe_set_gemm_tile.
 //
 // The tile scheduler, tile order and failure handling (bounded waits, drains,
 // TMEM freed on every path) are those of the bf16 kernel in gemm_tc.cu.

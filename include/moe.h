@@ -197,10 +197,10 @@ moe_status moe_route_permute(const float *logits, int T, int E, int S, int k, in
  * MOE_TILE_128x128 (up to 64 rows per group), MOE_TILE_128x256 (up to 128),
  * MOE_TILE_PAIR (256 x 256 tiles on CTA pairs, above).  int8 weights:
  * 256 weight rows x 16 / 32 / 64 tokens (MOE_TILE_W8_D16 up to 10 rows per
- * group, _D32 up to 24, _D64 up to 64), above that MOE_TILE_W8_PAIR (256
- * weight rows widened into tensor memory x up to 192 tokens on CTA pairs,
- * when H and I are multiples of 64) or else MOE_TILE_W8_ROWS (128 token
- * rows x 256 weight rows).  A forced tile of the other weight type leaves
+ * group, _D32 up to 24, _D64 below 64), from 64 rows per group
+ * MOE_TILE_W8_PAIR (256 weight rows widened into tensor memory x up to 192
+ * tokens on CTA pairs, when H and I are multiples of 64) or else
+ * MOE_TILE_W8_ROWS (128 token rows x 256 weight rows).  A forced tile of the other weight type leaves
  * that type's choice automatic.  Not synchronised with calls in flight on
  * other host threads; the results of every tile are within the same bounds
  * of the exact layer.  Returns MOE_ERR_INVALID_ARG for an unknown value.
