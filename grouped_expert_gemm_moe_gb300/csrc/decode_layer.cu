@@ -147,33 +147,60 @@ __global__ void __launch_bounds__(DL_THREADS, 2) decode_layer_kernel(
             }
         }
     }
+    // The down weights do not depend on h: each warp loads the first chunks
+    // of its first phase-2 task now, so that they are in flight while the
+    // other warps finish phase 1 and the grid meets at the barrier.
+    const int chunks2 = I / 8;
+    const int nblk2 = (H + DL_DOWN_RW - 1) / DL_DOWN_RW;
+    const int64_t ntasks2 = static_cast<int64_t>(na) * nblk2;
+    uint4 first[DL_DOWN_RW][4];
+    if (gwarp < ntasks2) {
+        const int a = static_cast<int>(gwarp / nblk2);
+        const int n0 = static_cast<int>(gwarp % nblk2) * DL_DOWN_RW;
+        down_load_first<4, DL_DOWN_RW>(w_down + (static_cast<int64_t>(pl.group[a]) * H + n0) * I,
+                                       I, n0, H, chunks2, pol, first);
+    }
     if (!grid_barrier(barrier, gridDim.x, &pl.fail, dev_error)) return;
 
     // ---------------------------------------------------------- phase 2
     {
-        const int chunks = I / 8;
-        const int nblk = (H + DL_DOWN_RW - 1) / DL_DOWN_RW;
-        const int64_t ntasks = static_cast<int64_t>(na) * nblk;
-        for (int64_t task = gwarp; task < ntasks; task += nwarps) {
+        const int chunks = chunks2;
+        const int nblk = nblk2;
+        auto store_y = [&](const float (&acc)[1][DL_DOWN_RW], int row, int n0) {
+#pragma unroll
+            for (int w = 0; w < DL_DOWN_RW; ++w) {
+                const float v = warp_sum(acc[0][w]);
+                if (lane == 0 && n0 + w < H) {
+                    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+                    y[static_cast<int64_t>(row) * H + n0 + w] =
+                        *reinterpret_cast<const uint16_t *>(&b);
+                }
+            }
+        };
+        auto task_rows = [&](int64_t task, int rfirst) {
             const int a = static_cast<int>(task / nblk);
             const int n0 = static_cast<int>(task % nblk) * DL_DOWN_RW;
             const int g = pl.group[a], r0 = pl.row0[a], nr = pl.row0[a + 1] - r0;
             const uint16_t *wd = w_down + (static_cast<int64_t>(g) * H + n0) * I;
-            for (int r = 0; r < nr; ++r) {
+            for (int r = rfirst; r < nr; ++r) {
                 float acc[1][DL_DOWN_RW];
                 down_partial_bf16<4, DL_DOWN_RW, 1, true>(h + static_cast<int64_t>(r0 + r) * I,
                                                           I, 1, wd, n0, H, chunks, pol, acc);
-#pragma unroll
-                for (int w = 0; w < DL_DOWN_RW; ++w) {
-                    const float v = warp_sum(acc[0][w]);
-                    if (lane == 0 && n0 + w < H) {
-                        const __nv_bfloat16 b = __float2bfloat16_rn(v);
-                        y[static_cast<int64_t>(r0 + r) * H + n0 + w] =
-                            *reinterpret_cast<const uint16_t *>(&b);
-                    }
-                }
+                store_y(acc, r0 + r, n0);
             }
+        };
+        if (gwarp < ntasks2) {          // this warp's first task: its first chunks are loaded
+            const int a = static_cast<int>(gwarp / nblk);
+            const int n0 = static_cast<int>(gwarp % nblk) * DL_DOWN_RW;
+            const int r0 = pl.row0[a];
+            const uint16_t *wd = w_down + (static_cast<int64_t>(pl.group[a]) * H + n0) * I;
+            float acc[1][DL_DOWN_RW];
+            down_partial_bf16_first<4, DL_DOWN_RW, true>(h + static_cast<int64_t>(r0) * I, I, wd,
+                                                         n0, H, chunks, pol, first, acc);
+            store_y(acc, r0, n0);
+            task_rows(gwarp, 1);        // its other hidden rows (T > 1)
         }
+        for (int64_t task = gwarp + nwarps; task < ntasks2; task += nwarps) task_rows(task, 0);
     }
     if (!grid_barrier(barrier, 2u * gridDim.x, &pl.fail, dev_error)) return;
     pdl_trigger();

@@ -118,4 +118,74 @@ __device__ __forceinline__ void down_partial_bf16(const uint16_t *hr, int I, int
     }
 }
 
+// The weights of the first 32 * NCH chunks of a down task (what
+// down_partial_bf16 loads first), for a caller that issues them early.
+template <int NCH, int RW>
+__device__ __forceinline__ void down_load_first(const uint16_t *wd, int I, int n0, int H,
+                                                int chunks, uint64_t pol, uint4 (&vw)[RW][NCH]) {
+    const int lane = lane_id();
+#pragma unroll
+    for (int u = 0; u < NCH; ++u) {
+        const int q = lane + 32 * u;
+        if (q < chunks) {
+#pragma unroll
+            for (int w = 0; w < RW; ++w)
+                if (n0 + w < H) vw[w][u] = ld_stream(wd + static_cast<int64_t>(w) * I + q * 8, pol);
+        }
+    }
+}
+
+// down_partial_bf16 for one hidden row whose first 32 * NCH weight chunks
+// are already in `first` (from down_load_first): the same loads after
+// those and the same sums in the same order.
+template <int NCH, int RW, bool H_COHERENT>
+__device__ __forceinline__ void down_partial_bf16_first(const uint16_t *hr, int I,
+                                                        const uint16_t *wd, int n0, int H,
+                                                        int chunks, uint64_t pol,
+                                                        const uint4 (&first)[RW][NCH],
+                                                        float (&acc)[1][RW]) {
+    const int lane = lane_id();
+#pragma unroll
+    for (int w = 0; w < RW; ++w) acc[0][w] = 0.f;
+    auto segment = [&](int seg, const uint4 (&vw)[RW][NCH], const uint4 (&vx)[NCH]) {
+#pragma unroll
+        for (int u = 0; u < NCH; ++u) {
+            if (seg + lane + 32 * u >= chunks) continue;
+            float fx[8];
+            unpack8(vx[u], fx);
+#pragma unroll
+            for (int w = 0; w < RW; ++w) {
+                if (n0 + w >= H) break;
+                float fw[8];
+                unpack8(vw[w][u], fw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[0][w] = fmaf(fw[e], fx[e], acc[0][w]);
+            }
+        }
+    };
+    {                                            // chunks 0 .. 32 NCH - 1: weights in `first`
+        uint4 vx[NCH];
+#pragma unroll
+        for (int u = 0; u < NCH; ++u) {
+            const int q = lane + 32 * u;
+            if (q < chunks) vx[u] = H_COHERENT ? ld_cg(hr + q * 8) : ld_nc(hr + q * 8);
+        }
+        segment(0, first, vx);
+    }
+    for (int seg = 32 * NCH; seg < chunks; seg += 32 * NCH) {
+        uint4 vw[RW][NCH], vx[NCH];
+#pragma unroll
+        for (int u = 0; u < NCH; ++u) {
+            const int q = seg + lane + 32 * u;
+            if (q < chunks) {
+#pragma unroll
+                for (int w = 0; w < RW; ++w)
+                    if (n0 + w < H) vw[w][u] = ld_stream(wd + static_cast<int64_t>(w) * I + q * 8, pol);
+                vx[u] = H_COHERENT ? ld_cg(hr + q * 8) : ld_nc(hr + q * 8);
+            }
+        }
+        segment(seg, vw, vx);
+    }
+}
+
 }  // namespace moe
