@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(PW_THREADS, 1)
         // ------------------------------------------- MMA issuer (CTA 0 only)
         if (leader && lane == 0) {
             int tb = 0, acc = 0, seq = 0;
-            uint32_t tph = 0, acc_ph = 0;
+            uint32_t acc_ph = 0;
             bool ok = true;
             const uint64_t dX = sw128_kmajor_desc(smem_u32(sX));
             for (int t = t_first, i = 0; t < total && ok; t += t_step, ++i) {
@@ -425,14 +425,13 @@ __global__ void __launch_bounds__(PW_THREADS, 1)
                     }
                     tc_commit_pair_both(&a_empty[s]);
                     tc_commit_pair_both(&b_empty[tb]);
-                    if (++tb == PW_TOK_STAGES) { tb = 0; tph ^= 1u; }
+                    if (++tb == PW_TOK_STAGES) tb = 0;
                 }
                 if (!ok) break;
                 tc_commit_pair_both(&accf[acc]);
                 acc ^= 1;
                 if (acc == 0) acc_ph ^= 1u;
             }
-            (void)tph;
             tc_commit_pair_local(drain);
             mbar_wait(drain, 0, dev_error);
         }
